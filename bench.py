@@ -1,0 +1,474 @@
+"""Routed-attention throughput benchmark (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 720p|1080p|480p]
+                    [--impl ours|reference]
+
+A step is one steady-state pass of the hot path for one layer: the fused
+append/evict of the current block's K/V into the restructured cache
+(hc_cache_append) followed by routed attention of the block's queries
+(hc_routed_attention).  The cache was built by the one-time pipeline
+(hc_classify on the window that just filled, then hc_cache_restructure),
+which is timed separately, as is the in-house full attention
+(hc_full_attention) on the same queries and window.
+
+value     query tokens/s over the K timed steps, inputs resident in HBM,
+          L2 flushed (512 MB write) before every step, CUDA events on the
+          launching stream; the sum over ranks for N > 1 (replicas, weak
+          scaling, no collective on the data path).
+e2e       the same metric through the same calls with HOST buffers: each
+          step copies Q and the block's K/V from pinned host memory and
+          copies O back, inside the timed region.
+roofline  the routed-attention kernel: algorithmic FLOPs per launch
+          (4*Nq*|keys|*d per head over its own key set) / its mean event
+          time, against the measured dense bf16 peak.
+cpu_baseline  the fp64 NumPy oracle on a bounded sample of the same step
+          (rank 0 only).
+
+--impl reference runs that oracle as the benchmark's reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "routed-attention query tokens/s at 720P/1080P shapes; x vs own full-attn; %roofline"
+UNIT = "query-tok/s"
+FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="720p", choices=["480p", "720p", "1080p"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_config(shape):
+    mix = "".join("SDPG"[a] for a in shape.mix)
+    return {"workload": f"{shape.name} layer", "n_heads": shape.n_heads, "head_dim": shape.head_dim,
+            "frame": f"{shape.frame_h}x{shape.frame_w}", "block_frames": shape.frames_per_block,
+            "window_frames": shape.window_frames, "query_tokens": shape.n_q,
+            "window_keys": shape.n_k, "head_mix": mix,
+            "step": "hc_cache_append + hc_routed_attention",
+            "l2": "flushed before every step (512 MB write)",
+            "parallelism": "replicas (one independent layer per GPU)"}
+
+
+def routed_flops(shape, labels):
+    """Algorithmic FLOPs of routed attention: 4*|q|*|keys|*d per (query, head)."""
+    F, d, nq = shape.frame_tokens, shape.head_dim, shape.n_q
+    total = 0
+    for a in labels:
+        if a in (synth.SINK, synth.DUMMY):
+            keys = nq * shape.n_q
+        elif a == synth.GLOBAL:
+            keys = nq * shape.n_k
+        else:
+            keys = 0
+            for hz in _cells(shape.frame_h):
+                for wz in _cells(shape.frame_w):
+                    c = hz * wz
+                    keys += (shape.frames_per_block * c) * (shape.window_frames * c)
+        total += 4 * keys * d
+    return total
+
+
+def _cells(n, c=10):
+    k = max(1, int(n / c + 0.5))
+    return [c] * (k - 1) + [n - c * (k - 1)]
+
+
+def routed_bytes(shape, labels, esize=2):
+    """Algorithmic bytes: every head's key set K and V read once, Q read once, O written once."""
+    F, d, nq = shape.frame_tokens, shape.head_dim, shape.n_q
+    kv = 0
+    for a in labels:
+        rows = nq if a in (synth.SINK, synth.DUMMY) else shape.n_k
+        kv += 2 * rows * d * esize
+    return kv + 2 * nq * shape.n_heads * d * esize
+
+
+class ClockSampler:
+    """nvidia-smi samples taken while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.25)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return j.get("bf16_tflops", 1800.0), j.get("hbm_gbs", 6400.0), "measured"
+    return 1800.0, 6400.0, "fallback"
+
+
+def traffic_from_profile(kernel_tag):
+    """Per-launch DRAM bytes recorded by an ncu capture of the current kernel
+    source, or None if none matches."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "head_routed_kv_classify_b300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(src)):
+        if name.endswith((".cu", ".h", ".cuh")):
+            with open(os.path.join(src, name), "rb") as f:
+                h.update(f.read())
+    digest = h.hexdigest()[:16]
+    tb, sha = None, None
+    for line in open(path):
+        if line.startswith("traffic_bytes_per_launch:"):
+            tb = float(line.split(":", 1)[1].split()[0])
+        if line.startswith("csrc_sha256_16:"):
+            sha = line.split(":", 1)[1].strip()
+    return tb if (tb is not None and sha == digest) else None
+
+
+# --------------------------------------------------------------------------- oracle arms
+
+def oracle_step_sample(shape, inp, labels, n_queries, seed):
+    from oracle import headcast_ref as ref
+    geom = ref.geometry_of(shape)
+    cache = ref.CacheModel(geom)
+    blk = shape.n_q
+    for b in range(shape.blocks_per_window):
+        cache.put(b, inp.k.values[b * blk:(b + 1) * blk], inp.v.values[b * blk:(b + 1) * blk])
+    idx = np.sort(np.random.default_rng(seed).choice(shape.n_q, n_queries, replace=False))
+    t0 = time.perf_counter()
+    ref.routed_attention(inp.q.values, cache, labels, query_idx=idx)
+    return time.perf_counter() - t0
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(shape, inp, labels, seconds):
+    """The oracle as it stands, on growing query samples until ~seconds of work."""
+    done, spent, n = 0, 0.0, 16
+    seed = 0
+    while spent < seconds:
+        spent += oracle_step_sample(shape, inp, labels, n, seed)
+        done += n
+        seed += 1
+        n = min(2 * n, 256)
+    return {"value": done / spent, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{done} query tokens (all {shape.n_heads} heads, routed key sets) of the "
+                      f"{shape.name} layer, fp64 NumPy, {spent:.1f} s"}
+
+
+def run_reference(args, shape, rank, world):
+    if rank != 0:
+        return
+    inp = synth.make_layer(shape)
+    labels = np.array(shape.mix, np.int8)
+    nq = 64
+    for s in range(args.warmup):
+        oracle_step_sample(shape, inp, labels, nq, 1000 + s)
+    t = 0.0
+    for s in range(args.steps):
+        t += oracle_step_sample(shape, inp, labels, nq, s)
+    value = nq * args.steps / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(shape),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"{nq} query tokens per step (all heads, routed key sets)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, shape, rank, world, local_rank):
+    import torch
+    import head_routed_kv_classify_b300 as hc
+    from head_routed_kv_classify_b300 import build as hcb
+
+    if not os.path.exists(hc.LIB_PATH):
+        hcb.build()
+    hc.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def to_dev(x):
+        return torch.from_numpy(x.raw.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+
+    inp = synth.make_layer(shape, seed=shape.seed + 1000 * rank)
+    q, k, v = to_dev(inp.q), to_dev(inp.k), to_dev(inp.v)
+    cfg = hc.config_for(shape)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    # One-time pipeline: classify the window that just filled, then restructure.
+    scratch = torch.empty(hc.hc_classify_scratch_bytes(cfg), dtype=torch.uint8, device=dev)
+    labels_dev = torch.empty(shape.n_heads, dtype=torch.int8, device=dev)
+    stats_dev = torch.empty((shape.n_heads, 6), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        hc.hc_classify(cfg, q, k, v, labels_dev=labels_dev, stats_dev=stats_dev, scratch=scratch,
+                       copy_labels=False)
+    flush.zero_()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    labels, _, _ = hc.hc_classify(cfg, q, k, v, labels_dev=labels_dev, stats_dev=stats_dev,
+                                  scratch=scratch)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    classify_ms = e0.elapsed_time(e1)
+    if list(labels) != list(shape.mix):
+        raise RuntimeError(f"classification gave {list(labels)}, planted {list(shape.mix)}")
+    cache = hc.hc_cache_create(cfg, labels, device=dev)
+    flush.zero_()
+    e0.record(stream)
+    cache.restructure(k, v, 0)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    restructure_ms = e0.elapsed_time(e1)
+
+    # Steady-state inputs: two fresh blocks alternate (4 denoising steps per block).
+    blocks = [synth.make_block(shape, seed=shape.seed + 77 + i + 1000 * rank) for i in range(2)]
+    qb = [to_dev(b[0]) for b in blocks]
+    kb = [to_dev(b[1]) for b in blocks]
+    vb = [to_dev(b[2]) for b in blocks]
+    o = torch.empty_like(q)
+    state = {"step": 0}
+    first_block = shape.blocks_per_window
+
+    def block_id():
+        return first_block + state["step"] // 4
+
+    def step(i, evs):
+        flush.zero_()
+        s0, s1, r0 = evs
+        s0.record(stream)
+        cache.append(block_id(), kb[i % 2], vb[i % 2])
+        r0.record(stream)
+        cache.routed_attention(qb[i % 2], o)
+        s1.record(stream)
+        state["step"] += 1
+
+    for i in range(args.warmup):
+        step(i, (ev(), ev(), ev()))
+    torch.cuda.synchronize()
+    hc.hc_get_last_error()
+
+    clock = ClockSampler(local_rank) if rank == 0 else None
+    if clock:
+        clock.start()
+    evs = [(ev(), ev(), ev()) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i, evs[i])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = clock.stop() if clock else None
+    hc.hc_get_last_error()
+    step_ms = [a.elapsed_time(b) for a, b, _ in evs]
+    routed_ms = [r.elapsed_time(b) for _, b, r in evs]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # In-house full attention on the same queries over the monolithic window,
+    # plus the monolithic-ring append it needs (one contiguous copy per block).
+    k_ring, v_ring = k.clone(), v.clone()
+    full_ms, mono_ms = [], []
+    nfull = max(5, min(args.steps, 30))
+    for i in range(args.warmup + nfull):
+        flush.zero_()
+        a0, a1, a2 = ev(), ev(), ev()
+        a0.record(stream)
+        slot = (first_block + i // 4) % shape.blocks_per_window
+        rows = slice(slot * shape.n_q, (slot + 1) * shape.n_q)
+        k_ring[rows].copy_(kb[i % 2], non_blocking=True)
+        v_ring[rows].copy_(vb[i % 2], non_blocking=True)
+        a1.record(stream)
+        hc.hc_full_attention(cfg, qb[i % 2], k_ring, v_ring, o=o)
+        a2.record(stream)
+        if i >= args.warmup:
+            full_ms.append((a1, a2))
+            mono_ms.append((a0, a1))
+    torch.cuda.synchronize()
+    full_ms = [a.elapsed_time(b) for a, b in full_ms]
+    mono_ms = [a.elapsed_time(b) for a, b in mono_ms]
+
+    # End to end through the same public calls from pinned host buffers.
+    e2e = None
+    if args.e2e_steps > 0:
+        hq = [b.pin_memory() for b in (x.cpu() for x in qb)]
+        hk = [b.pin_memory() for b in (x.cpu() for x in kb)]
+        hv = [b.pin_memory() for b in (x.cpu() for x in vb)]
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(kb[0]), torch.empty_like(vb[0])
+        times = []
+        for i in range(args.warmup + args.e2e_steps):
+            flush.zero_()
+            a0, a1 = ev(), ev()
+            a0.record(stream)
+            dq.copy_(hq[i % 2], non_blocking=True)
+            dk.copy_(hk[i % 2], non_blocking=True)
+            dv.copy_(hv[i % 2], non_blocking=True)
+            cache.append(block_id(), dk, dv)
+            cache.routed_attention(dq, o)
+            ho.copy_(o, non_blocking=True)
+            a1.record(stream)
+            state["step"] += 1
+            if i >= args.warmup:
+                times.append((a0, a1))
+        torch.cuda.synchronize()
+        times = [a.elapsed_time(b) for a, b in times]
+        nb = q.numel() * q.element_size()
+        e2e = {"value": world * shape.n_q / (1e-3 * statistics.mean(times)), "unit": UNIT,
+               "h2d_bytes_per_step": 3 * nb, "d2h_bytes_per_step": nb,
+               "ms_per_step": statistics.mean(times)}
+
+    if rank != 0:
+        return
+    peak_tf, peak_bw, peak_kind = measured_peaks()
+    flops = routed_flops(shape, labels)
+    mean_routed = statistics.mean(routed_ms)
+    achieved = flops / (mean_routed * 1e-3) / 1e12
+    tb = traffic_from_profile(f"routed_attention_{shape.name}")
+    value = world * shape.n_q * args.steps / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V with planted archetypes; pages' 720P shapes)",
+        "config": workload_config(shape),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": tb,
+                     "kernel": "routed attention (one launch, all heads)",
+                     "algorithmic_flops_per_launch": flops,
+                     "algorithmic_bytes_per_launch": routed_bytes(shape, labels),
+                     "peak_source": f"{peak_kind} bf16 dense (burst)"},
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "routed_attention_ms": mean_routed,
+        "append_ms": statistics.mean(s - r for s, r in zip(step_ms, routed_ms)),
+        "full_attention_ms": statistics.mean(full_ms),
+        "monolithic_append_ms": statistics.mean(mono_ms),
+        "speedup_vs_full_attention": statistics.mean(full_ms) / mean_routed,
+        "step_speedup_vs_full": (statistics.mean(full_ms) + statistics.mean(mono_ms)) /
+                                (total_ms / args.steps),
+        "classify_ms": classify_ms, "restructure_ms": restructure_ms,
+        "wall_s_timed": wall,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, inp, labels, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    shape = synth.SHAPES[args.workload]
+    if args.impl == "reference":
+        run_reference(args, shape, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    run_ours(args, shape, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,313 @@
+"""Python binding of libheadcast.so (head-routed attention for AR video DiTs).
+
+Argument marshalling only: every step of classification, cache maintenance
+and attention runs in the library's CUDA kernels.  PyTorch supplies device
+memory and streams; tensors are passed by ``data_ptr()``.  There is no CPU
+fallback: if the shared library is missing, importing the compute functions
+raises ``HeadcastUnavailable``.
+
+Names mirror the C ABI in include/headcast.h:
+    hc_config_default, hc_config_validate, hc_classify_scratch_bytes,
+    hc_classify, hc_cache_bytes, hc_cache_create (-> Cache),
+    hc_cache_restructure, hc_cache_append, hc_routed_attention,
+    hc_full_attention, hc_get_last_error
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libheadcast.so")
+
+SINK, DUMMY, SPATIAL, GLOBAL = 0, 1, 2, 3
+ARCHETYPES = ("sink", "dummy", "spatial", "global")
+HC_BF16, HC_FP32 = 0, 1
+STATUS_NAMES = {0: "HC_OK", 1: "HC_ERR_INVALID_ARG", 2: "HC_ERR_SHAPE", 3: "HC_ERR_DTYPE",
+                4: "HC_ERR_ALIGN", 5: "HC_ERR_STATE", 6: "HC_ERR_CUDA", 7: "HC_ERR_TIMEOUT",
+                8: "HC_ERR_UNSUPPORTED", 9: "HC_ERR_SIZE"}
+MAX_HEADS = 64
+
+# Every symbol include/headcast.h declares.
+EXPORTS = ("hc_abi_version", "hc_status_string", "hc_last_error_message", "hc_config_default",
+           "hc_config_validate", "hc_classify_scratch_bytes", "hc_classify", "hc_cache_bytes",
+           "hc_cache_create", "hc_cache_destroy", "hc_cache_get_info", "hc_cache_restructure",
+           "hc_cache_append", "hc_routed_attention", "hc_full_attention", "hc_get_last_error")
+
+
+class HeadcastUnavailable(RuntimeError):
+    pass
+
+
+class HeadcastError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{self.name}: {message}")
+
+
+class HcConfig(C.Structure):
+    _fields_ = [("n_heads", C.c_int32), ("head_dim", C.c_int32), ("frame_h", C.c_int32),
+                ("frame_w", C.c_int32), ("frames_per_block", C.c_int32),
+                ("window_frames", C.c_int32), ("dtype", C.c_int32), ("softmax_scale", C.c_float),
+                ("theta_sink", C.c_float), ("theta_dummy", C.c_float),
+                ("theta_spatial", C.c_float), ("theta_score", C.c_float), ("gamma", C.c_float),
+                ("proxy_radius", C.c_int32), ("cell_h", C.c_int32), ("cell_w", C.c_int32)]
+
+    @property
+    def F(self):
+        return self.frame_h * self.frame_w
+
+    @property
+    def block_tokens(self):
+        return self.frames_per_block * self.F
+
+
+class HcCacheInfo(C.Structure):
+    _fields_ = [("newest_block", C.c_int64), ("valid_frames", C.c_int32),
+                ("sink_present", C.c_int32), ("n_by_archetype", C.c_int32 * 4),
+                ("rows_by_archetype", C.c_int64 * 4), ("bytes", C.c_size_t),
+                ("monolithic_bytes", C.c_size_t)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the shared library (no GPU needed) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise HeadcastUnavailable(f"{path} is not built; run head_routed_kv_classify_b300.build")
+    lib = C.CDLL(path)
+    vp, i32, i64, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
+    cfgp = C.POINTER(HcConfig)
+    sig = {
+        "hc_abi_version": (i32, []),
+        "hc_status_string": (C.c_char_p, [C.c_int]),
+        "hc_last_error_message": (C.c_char_p, []),
+        "hc_config_default": (C.c_int, [cfgp]),
+        "hc_config_validate": (C.c_int, [cfgp]),
+        "hc_classify_scratch_bytes": (C.c_int, [cfgp, i32, C.POINTER(sz)]),
+        "hc_classify": (C.c_int, [cfgp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
+        "hc_cache_bytes": (C.c_int, [cfgp, vp, C.POINTER(sz)]),
+        "hc_cache_create": (C.c_int, [cfgp, vp, vp, sz, C.POINTER(vp)]),
+        "hc_cache_destroy": (C.c_int, [vp]),
+        "hc_cache_get_info": (C.c_int, [vp, C.POINTER(HcCacheInfo)]),
+        "hc_cache_restructure": (C.c_int, [vp, vp, vp, i64, i32, vp]),
+        "hc_cache_append": (C.c_int, [vp, i64, vp, vp, vp]),
+        "hc_routed_attention": (C.c_int, [vp, vp, vp, vp]),
+        "hc_full_attention": (C.c_int, [cfgp, vp, vp, vp, i32, i32, vp, vp]),
+        "hc_get_last_error": (C.c_int, [vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status):
+    if status != 0:
+        msg = load().hc_last_error_message().decode(errors="replace")
+        raise HeadcastError(status, msg)
+
+
+# ----------------------------------------------------------------- config
+
+def hc_config_default() -> HcConfig:
+    cfg = HcConfig()
+    _check(load().hc_config_default(C.byref(cfg)))
+    return cfg
+
+
+def make_config(n_heads, head_dim, frame_h, frame_w, window_frames=21, dtype="bf16",
+                frames_per_block=3, **overrides) -> HcConfig:
+    cfg = hc_config_default()
+    cfg.n_heads, cfg.head_dim, cfg.frame_h, cfg.frame_w = n_heads, head_dim, frame_h, frame_w
+    cfg.window_frames, cfg.frames_per_block = window_frames, frames_per_block
+    cfg.dtype = {"bf16": HC_BF16, "fp32": HC_FP32}[dtype] if isinstance(dtype, str) else int(dtype)
+    for k, v in overrides.items():
+        setattr(cfg, k, v)
+    return cfg
+
+
+def config_for(shape, **overrides) -> HcConfig:
+    """Config from any object with the synthetic-layer fields."""
+    return make_config(shape.n_heads, shape.head_dim, shape.frame_h, shape.frame_w,
+                       shape.window_frames, shape.dtype, shape.frames_per_block, **overrides)
+
+
+def hc_config_validate(cfg: HcConfig):
+    _check(load().hc_config_validate(C.byref(cfg)))
+
+
+# ----------------------------------------------------------------- helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    if stream is None:
+        return C.c_void_p(_torch().cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return C.c_void_p(stream)
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _dtype_of(cfg):
+    t = _torch()
+    return t.bfloat16 if cfg.dtype == HC_BF16 else t.float32
+
+
+def _ptr(t, cfg=None, name="tensor", shape=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if cfg is not None and t.dtype != _dtype_of(cfg):
+        raise ValueError(f"{name} has dtype {t.dtype}, config wants {_dtype_of(cfg)}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return C.c_void_p(t.data_ptr())
+
+
+# ----------------------------------------------------------------- classification
+
+def hc_classify_scratch_bytes(cfg, n_key_frames=None) -> int:
+    n = C.c_size_t(0)
+    nkf = cfg.window_frames if n_key_frames is None else n_key_frames
+    _check(load().hc_classify_scratch_bytes(C.byref(cfg), nkf, C.byref(n)))
+    return n.value
+
+
+def hc_classify(cfg, q, k, v, n_key_frames=None, labels_dev=None, stats_dev=None, o_full=None,
+                scratch=None, stream=None, copy_labels=True):
+    """Classify every head.  Returns (labels_host int8[H] or None, labels_dev,
+    stats_dev [H][6]: c_sink, c_dummy, c_spatial, P5, MSE, score)."""
+    t = _torch()
+    nkf = cfg.window_frames if n_key_frames is None else n_key_frames
+    H, d = cfg.n_heads, cfg.head_dim
+    dev = q.device
+    if labels_dev is None:
+        labels_dev = t.empty(H, dtype=t.int8, device=dev)
+    if stats_dev is None:
+        stats_dev = t.empty((H, 6), dtype=t.float32, device=dev)
+    nbytes = hc_classify_scratch_bytes(cfg, nkf)
+    if scratch is None:
+        scratch = t.empty(nbytes, dtype=t.uint8, device=dev)
+    host = np.zeros(H, dtype=np.int8) if copy_labels else None
+    _check(load().hc_classify(
+        C.byref(cfg), _ptr(q, cfg, "q", (cfg.block_tokens, H, d)),
+        _ptr(k, cfg, "k", (nkf * cfg.F, H, d)), _ptr(v, cfg, "v", (nkf * cfg.F, H, d)), nkf,
+        _ptr(labels_dev, None, "labels_dev"),
+        host.ctypes.data_as(C.c_void_p) if host is not None else None,
+        _ptr(stats_dev, None, "stats_dev"), _ptr(o_full, cfg, "o_full"),
+        _ptr(scratch, None, "scratch"), scratch.numel() * scratch.element_size(), _stream(stream)))
+    return host, labels_dev, stats_dev
+
+
+# ----------------------------------------------------------------- cache
+
+def hc_cache_bytes(cfg, labels) -> int:
+    lab = np.ascontiguousarray(np.asarray(labels, dtype=np.int8))
+    n = C.c_size_t(0)
+    _check(load().hc_cache_bytes(C.byref(cfg), lab.ctypes.data_as(C.c_void_p), C.byref(n)))
+    return n.value
+
+
+class Cache:
+    """A restructured per-archetype cache: the library's handle plus the
+    caller-owned backing buffer (a torch uint8 tensor)."""
+
+    def __init__(self, cfg, labels, device=None, buf=None):
+        t = _torch()
+        self.cfg = cfg
+        self.labels = np.ascontiguousarray(np.asarray(labels, dtype=np.int8))
+        self.nbytes = hc_cache_bytes(cfg, self.labels)
+        if buf is None:
+            buf = t.empty(self.nbytes + 256, dtype=t.uint8, device=device or "cuda")
+        base = buf.data_ptr()
+        self._buf = buf
+        self._off = (-base) % 256
+        handle = C.c_void_p(0)
+        _check(load().hc_cache_create(C.byref(cfg), self.labels.ctypes.data_as(C.c_void_p),
+                                      C.c_void_p(base + self._off),
+                                      buf.numel() - self._off, C.byref(handle)))
+        self.handle = handle
+
+    def close(self):
+        if self.handle:
+            load().hc_cache_destroy(self.handle)
+            self.handle = C.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def info(self) -> dict:
+        inf = HcCacheInfo()
+        _check(load().hc_cache_get_info(self.handle, C.byref(inf)))
+        return dict(newest_block=inf.newest_block, valid_frames=inf.valid_frames,
+                    sink_present=bool(inf.sink_present),
+                    n_by_archetype=list(inf.n_by_archetype),
+                    rows_by_archetype=list(inf.rows_by_archetype), bytes=inf.bytes,
+                    monolithic_bytes=inf.monolithic_bytes)
+
+    def restructure(self, k_win, v_win, first_block_id=0, n_blocks=None, stream=None):
+        cfg = self.cfg
+        nb = k_win.shape[0] // cfg.block_tokens if n_blocks is None else n_blocks
+        shape = (nb * cfg.block_tokens, cfg.n_heads, cfg.head_dim)
+        _check(load().hc_cache_restructure(self.handle, _ptr(k_win, cfg, "k_win", shape),
+                                           _ptr(v_win, cfg, "v_win", shape), first_block_id, nb,
+                                           _stream(stream)))
+
+    def append(self, block_id, k_blk, v_blk, stream=None):
+        cfg = self.cfg
+        shape = (cfg.block_tokens, cfg.n_heads, cfg.head_dim)
+        _check(load().hc_cache_append(self.handle, block_id, _ptr(k_blk, cfg, "k_blk", shape),
+                                      _ptr(v_blk, cfg, "v_blk", shape), _stream(stream)))
+
+    def routed_attention(self, q, o=None, stream=None):
+        cfg = self.cfg
+        shape = (cfg.block_tokens, cfg.n_heads, cfg.head_dim)
+        if o is None:
+            o = _torch().empty(shape, dtype=_dtype_of(cfg), device=q.device)
+        _check(load().hc_routed_attention(self.handle, _ptr(q, cfg, "q", shape),
+                                          _ptr(o, cfg, "o", shape), _stream(stream)))
+        return o
+
+
+def hc_cache_create(cfg, labels, device=None, buf=None) -> Cache:
+    return Cache(cfg, labels, device, buf)
+
+
+def hc_routed_attention(cache: Cache, q, o=None, stream=None):
+    return cache.routed_attention(q, o, stream)
+
+
+def hc_full_attention(cfg, q, k, v, o=None, n_key_frames=None, stream=None):
+    nkf = k.shape[0] // cfg.F if n_key_frames is None else n_key_frames
+    H, d = cfg.n_heads, cfg.head_dim
+    nq = q.shape[0]
+    if o is None:
+        o = _torch().empty((nq, H, d), dtype=_dtype_of(cfg), device=q.device)
+    _check(load().hc_full_attention(C.byref(cfg), _ptr(q, cfg, "q", (nq, H, d)),
+                                    _ptr(k, cfg, "k", (nkf * cfg.F, H, d)),
+                                    _ptr(v, cfg, "v", (nkf * cfg.F, H, d)), nq, nkf,
+                                    _ptr(o, cfg, "o", (nq, H, d)), _stream(stream)))
+    return o
+
+
+def hc_get_last_error(stream=None):
+    _check(load().hc_get_last_error(_stream(stream)))

@@ -1,0 +1,564 @@
+// Host side of the C ABI declared in include/headcast.h: argument checks,
+// the restructured cache's layout and work list, and kernel launches.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "hc_internal.h"
+
+using hc::Geom;
+using hc::HeadSlot;
+using hc::WorkItem;
+
+// Device status word: kernels record bounded-wait expiry or a failed bounds
+// check here instead of trapping; hc_get_last_error reads and clears it.
+__device__ int g_hc_status_word;
+
+struct hc_cache {
+  hc_config cfg;
+  Geom g;
+  int8_t labels[HC_MAX_HEADS];
+  HeadSlot heads[HC_MAX_HEADS];
+  char* buf;
+  size_t bytes, used, off_items, off_k, off_v;
+  int n_items;
+  int64_t rows;
+  int64_t rows_by_arch[4];
+  int n_by_arch[4];
+  int64_t newest;
+  int valid_frames;
+  bool sink_present;
+};
+
+namespace {
+
+thread_local std::string g_msg;
+
+hc_status fail(hc_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return s;
+}
+
+hc_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(HC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define HC_CUDA(call, what)                        \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t esize_of(int dtype) { return dtype == HC_FP32 ? 4 : 2; }
+
+Geom make_geom(const hc_config& c) {
+  Geom g;
+  g.H = c.n_heads;
+  g.d = c.head_dim;
+  g.Fh = c.frame_h;
+  g.Fw = c.frame_w;
+  g.F = c.frame_h * c.frame_w;
+  g.fpb = c.frames_per_block;
+  g.Wf = c.window_frames;
+  g.blk = g.fpb * g.F;
+  g.cell_h = c.cell_h;
+  g.cell_w = c.cell_w;
+  g.ncell_h = hc::n_cells(c.frame_h, c.cell_h);
+  g.ncell_w = hc::n_cells(c.frame_w, c.cell_w);
+  g.radius = c.proxy_radius;
+  const double scale = c.softmax_scale > 0.f ? (double)c.softmax_scale : 1.0 / std::sqrt((double)c.head_dim);
+  g.scale_log2 = (float)(scale * 1.4426950408889634);
+  return g;
+}
+
+// Address of the status word on the current device.
+hc_status status_ptr(int** out) {
+  static std::mutex mu;
+  static int* cached[128] = {nullptr};
+  int dev = 0;
+  HC_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= 128) return fail(HC_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    void* p = nullptr;
+    HC_CUDA(cudaGetSymbolAddress(&p, g_hc_status_word), "cudaGetSymbolAddress(status)");
+    cached[dev] = static_cast<int*>(p);
+  }
+  *out = cached[dev];
+  return HC_OK;
+}
+
+bool finite_all(std::initializer_list<float> xs) {
+  for (float x : xs)
+    if (!std::isfinite(x)) return false;
+  return true;
+}
+
+// Per-head rows of the restructured cache.
+int64_t head_rows(const Geom& g, int arch) {
+  return (arch == HC_SINK || arch == HC_DUMMY) ? (int64_t)g.blk : (int64_t)g.Wf * g.F;
+}
+
+struct Plan {
+  std::vector<WorkItem> items;
+  HeadSlot heads[HC_MAX_HEADS];
+  int64_t rows = 0;
+  int64_t rows_by_arch[4] = {0, 0, 0, 0};
+  int n_by_arch[4] = {0, 0, 0, 0};
+  size_t off_items = 0, off_k = 0, off_v = 0, bytes = 0;
+};
+
+hc_status check_labels(const hc_config* cfg, const int8_t* labels) {
+  if (!labels) return fail(HC_ERR_INVALID_ARG, "labels_host is null");
+  for (int h = 0; h < cfg->n_heads; ++h)
+    if (labels[h] < HC_SINK || labels[h] > HC_GLOBAL)
+      return fail(HC_ERR_INVALID_ARG, "label %d of head %d is not an archetype", labels[h], h);
+  return HC_OK;
+}
+
+// Cache layout and the routed work list.  Items are ordered by decreasing
+// work so that the hardware block scheduler approximates
+// longest-processing-time-first.
+void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
+  const Geom g = make_geom(cfg);
+  const int BM = hc::attention_block_rows(cfg.dtype, cfg.head_dim);
+  for (int h = 0; h < g.H; ++h) {
+    const int a = labels[h];
+    P.heads[h].arch = a;
+    P.heads[h].pad = 0;
+    P.heads[h].row0 = P.rows;
+    const int64_t r = head_rows(g, a);
+    P.rows += r;
+    P.rows_by_arch[a] += r;
+    P.n_by_arch[a] += 1;
+    auto push = [&](int kind, int q0, int nq, int64_t k_row0, int k_len, int k_per_frame, int cell) {
+      WorkItem w;
+      std::memset(&w, 0, sizeof w);
+      w.head = h;
+      w.kind = kind;
+      w.q0 = q0;
+      w.nq = nq;
+      w.k_row0 = k_row0;
+      w.k_len = k_len;
+      w.k_per_frame = k_per_frame;
+      w.cell = cell;
+      w.out_plane = 0;
+      P.items.push_back(w);
+    };
+    if (a == HC_SINK || a == HC_DUMMY) {
+      for (int q0 = 0; q0 < g.blk; q0 += BM)
+        push(hc::ITEM_RANGE, q0, std::min(BM, g.blk - q0), P.heads[h].row0, g.blk, 0, 0);
+    } else if (a == HC_GLOBAL) {
+      for (int q0 = 0; q0 < g.blk; q0 += BM)
+        push(hc::ITEM_RANGE, q0, std::min(BM, g.blk - q0), P.heads[h].row0, 0, g.F, 0);
+    } else {
+      for (int ci = 0; ci < g.ncell_h; ++ci)
+        for (int cj = 0; cj < g.ncell_w; ++cj) {
+          const int hz = hc::cell_extent(ci, g.Fh, g.cell_h, g.ncell_h);
+          const int wz = hc::cell_extent(cj, g.Fw, g.cell_w, g.ncell_w);
+          const int csz = hz * wz, nq = g.fpb * csz;
+          const int64_t k0 = P.heads[h].row0 + (int64_t)g.Wf * hc::cell_tokens_before(g, ci, cj);
+          for (int q0 = 0; q0 < nq; q0 += BM)
+            push(hc::ITEM_CELL, q0, std::min(BM, nq - q0), k0, 0, csz, ci * g.ncell_w + cj);
+        }
+    }
+  }
+  auto cost = [&](const WorkItem& w) {
+    const int64_t keys = w.k_per_frame > 0 ? (int64_t)w.k_per_frame * g.Wf : w.k_len;
+    return keys * w.nq;
+  };
+  std::stable_sort(P.items.begin(), P.items.end(),
+                   [&](const WorkItem& x, const WorkItem& y) { return cost(x) > cost(y); });
+  const size_t row_bytes = (size_t)g.d * esize_of(cfg.dtype);
+  P.off_items = 256;
+  P.off_k = round_up(P.off_items + P.items.size() * sizeof(WorkItem), 256);
+  P.off_v = round_up(P.off_k + (size_t)P.rows * row_bytes, 256);
+  P.bytes = round_up(P.off_v + (size_t)P.rows * row_bytes, 256);
+}
+
+}  // namespace
+
+// ===========================================================================
+
+extern "C" {
+
+int32_t hc_abi_version(void) { return HC_ABI_VERSION; }
+
+const char* hc_status_string(hc_status s) {
+  switch (s) {
+    case HC_OK: return "ok";
+    case HC_ERR_INVALID_ARG: return "invalid argument";
+    case HC_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case HC_ERR_DTYPE: return "unsupported dtype";
+    case HC_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case HC_ERR_STATE: return "call not valid in the current state";
+    case HC_ERR_CUDA: return "CUDA error";
+    case HC_ERR_TIMEOUT: return "device-side wait expired";
+    case HC_ERR_UNSUPPORTED: return "unsupported";
+    case HC_ERR_SIZE: return "buffer too small";
+  }
+  return "unknown status";
+}
+
+const char* hc_last_error_message(void) { return g_msg.c_str(); }
+
+hc_status hc_config_default(hc_config* out) {
+  if (!out) return fail(HC_ERR_INVALID_ARG, "out is null");
+  std::memset(out, 0, sizeof *out);
+  out->frames_per_block = 3;
+  out->window_frames = 21;
+  out->dtype = HC_BF16;
+  out->softmax_scale = 0.f;
+  out->theta_sink = 0.95f;
+  out->theta_dummy = 0.95f;
+  out->theta_spatial = 0.95f;
+  out->theta_score = 0.755f;
+  out->gamma = 5.f;
+  out->proxy_radius = 2;
+  out->cell_h = 10;
+  out->cell_w = 10;
+  return HC_OK;
+}
+
+hc_status hc_config_validate(const hc_config* c) {
+  if (!c) return fail(HC_ERR_INVALID_ARG, "config is null");
+  if (c->n_heads < 1 || c->n_heads > HC_MAX_HEADS)
+    return fail(HC_ERR_SHAPE, "n_heads %d not in 1..%d", c->n_heads, HC_MAX_HEADS);
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(HC_ERR_SHAPE, "head_dim %d not 64 or 128", c->head_dim);
+  if (c->frame_h < 1 || c->frame_w < 1 || c->frame_h > 4096 || c->frame_w > 4096)
+    return fail(HC_ERR_SHAPE, "frame %dx%d out of range", c->frame_h, c->frame_w);
+  if ((int64_t)c->frame_h * c->frame_w > (1 << 22))
+    return fail(HC_ERR_SHAPE, "frame of %lld tokens too large", (long long)c->frame_h * c->frame_w);
+  if (c->frames_per_block < 1 || c->frames_per_block > 64)
+    return fail(HC_ERR_SHAPE, "frames_per_block %d out of range", c->frames_per_block);
+  if (c->window_frames < c->frames_per_block || c->window_frames % c->frames_per_block != 0 ||
+      c->window_frames > 4096)
+    return fail(HC_ERR_SHAPE, "window_frames %d is not a positive multiple of frames_per_block %d",
+                c->window_frames, c->frames_per_block);
+  if ((int64_t)c->frames_per_block * c->frame_h * c->frame_w * c->n_heads * c->head_dim >= (1ll << 31) ||
+      (int64_t)c->frames_per_block * c->frame_h * c->frame_w >= (1 << 24))
+    return fail(HC_ERR_SHAPE, "block too large");
+  if (c->dtype != HC_BF16 && c->dtype != HC_FP32) return fail(HC_ERR_DTYPE, "dtype %d", c->dtype);
+  if (!finite_all({c->softmax_scale, c->theta_sink, c->theta_dummy, c->theta_spatial, c->theta_score, c->gamma}) ||
+      c->softmax_scale < 0.f)
+    return fail(HC_ERR_INVALID_ARG, "non-finite threshold or negative scale");
+  if (c->proxy_radius < 0 || c->cell_h < 1 || c->cell_w < 1)
+    return fail(HC_ERR_INVALID_ARG, "proxy_radius %d / cell %dx%d", c->proxy_radius, c->cell_h, c->cell_w);
+  return HC_OK;
+}
+
+// ------------------------------------------------------------ classification
+
+static void classify_layout(const hc_config& c, size_t* planes, size_t* tok, size_t* total) {
+  const int64_t nq = (int64_t)c.frames_per_block * c.frame_h * c.frame_w;
+  const size_t plane = (size_t)nq * c.n_heads * c.head_dim * sizeof(float);
+  *planes = plane;
+  *tok = round_up(4 * plane, 256);
+  *total = round_up(*tok + 4 * (size_t)c.n_heads * nq * sizeof(float), 256);
+}
+
+hc_status hc_classify_scratch_bytes(const hc_config* cfg, int32_t n_key_frames, size_t* bytes) {
+  hc_status s = hc_config_validate(cfg);
+  if (s != HC_OK) return s;
+  if (!bytes) return fail(HC_ERR_INVALID_ARG, "bytes is null");
+  (void)n_key_frames;
+  size_t pl, tk;
+  classify_layout(*cfg, &pl, &tk, bytes);
+  return HC_OK;
+}
+
+hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const void* v,
+                      int32_t n_key_frames, int8_t* labels_dev, int8_t* labels_host,
+                      float* stats_dev, void* o_full, void* scratch, size_t scratch_bytes,
+                      void* stream) {
+  hc_status s = hc_config_validate(cfg);
+  if (s != HC_OK) return s;
+  if (!q || !k || !v || !labels_dev || !scratch)
+    return fail(HC_ERR_INVALID_ARG, "q, k, v, labels_dev and scratch must be non-null");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(scratch) ||
+      (o_full && !aligned16(o_full)) || (stats_dev && !aligned16(stats_dev)))
+    return fail(HC_ERR_ALIGN, "device pointers must be 16-byte aligned");
+  if (n_key_frames < 2 * cfg->frames_per_block || n_key_frames % cfg->frames_per_block != 0 ||
+      n_key_frames > 4096)
+    return fail(HC_ERR_SHAPE, "n_key_frames %d must be a multiple of frames_per_block and hold >= 2 blocks",
+                n_key_frames);
+  size_t plane, tok_off, need;
+  classify_layout(*cfg, &plane, &tok_off, &need);
+  if (scratch_bytes < need) return fail(HC_ERR_SIZE, "scratch %zu < %zu bytes", scratch_bytes, need);
+  int* status = nullptr;
+  if ((s = status_ptr(&status)) != HC_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Geom g = make_geom(*cfg);
+  const int BM = hc::attention_block_rows(cfg->dtype, cfg->head_dim);
+  const int64_t nk = (int64_t)n_key_frames * g.F;
+
+  hc::AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = scratch;
+  p.k_stride = (int64_t)g.H * g.d;
+  p.k_hstride = g.d;
+  p.o_plane_stride = (int64_t)(plane / sizeof(float));
+  p.nq_total = g.blk;
+  p.out_fp32 = 1;
+  p.item_mode = hc::ITEMS_DENSE;
+  p.plane_k0[0] = 0;
+  p.plane_klen[0] = (int32_t)nk;
+  p.plane_k0[1] = 0;
+  p.plane_klen[1] = g.blk;
+  p.plane_k0[2] = nk - g.blk;
+  p.plane_klen[2] = g.blk;
+  p.g = g;
+  p.status = status;
+  HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3((g.blk + BM - 1) / BM, g.H, 3), st),
+          "classification attention");
+  p.item_mode = hc::ITEMS_PROXY;
+  p.proxy_frames = n_key_frames;
+  p.tiles_per_frame = (g.F + BM - 1) / BM;
+  HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3(g.fpb * p.tiles_per_frame, g.H, 1), st),
+          "classification proxy attention");
+
+  hc::ClassifyPost c;
+  std::memset(&c, 0, sizeof c);
+  c.planes = static_cast<const float*>(scratch);
+  c.plane_stride = p.o_plane_stride;
+  c.tok = reinterpret_cast<float*>(static_cast<char*>(scratch) + tok_off);
+  c.o_full = o_full;
+  c.o_full_fp32 = cfg->dtype == HC_FP32;
+  c.labels = labels_dev;
+  c.stats = stats_dev;
+  c.nq = g.blk;
+  c.g = g;
+  c.theta_sink = cfg->theta_sink;
+  c.theta_dummy = cfg->theta_dummy;
+  c.theta_spatial = cfg->theta_spatial;
+  c.theta_score = cfg->theta_score;
+  c.gamma = cfg->gamma;
+  HC_CUDA(hc::launch_classify_post(c, st), "classification statistics");
+  if (labels_host) {
+    HC_CUDA(cudaMemcpyAsync(labels_host, labels_dev, g.H, cudaMemcpyDeviceToHost, st), "label copy");
+    HC_CUDA(cudaStreamSynchronize(st), "stream synchronize");
+  }
+  return HC_OK;
+}
+
+// ------------------------------------------------------------ cache
+
+hc_status hc_cache_bytes(const hc_config* cfg, const int8_t* labels_host, size_t* bytes) {
+  hc_status s = hc_config_validate(cfg);
+  if (s != HC_OK) return s;
+  if ((s = check_labels(cfg, labels_host)) != HC_OK) return s;
+  if (!bytes) return fail(HC_ERR_INVALID_ARG, "bytes is null");
+  Plan P;
+  plan_cache(*cfg, labels_host, P);
+  *bytes = P.bytes;
+  return HC_OK;
+}
+
+hc_status hc_cache_create(const hc_config* cfg, const int8_t* labels_host, void* buf, size_t bytes,
+                          hc_cache** out) {
+  hc_status s = hc_config_validate(cfg);
+  if (s != HC_OK) return s;
+  if ((s = check_labels(cfg, labels_host)) != HC_OK) return s;
+  if (!buf || !out) return fail(HC_ERR_INVALID_ARG, "buf and out must be non-null");
+  if ((reinterpret_cast<uintptr_t>(buf) & 255u) != 0) return fail(HC_ERR_ALIGN, "buf must be 256-byte aligned");
+  Plan P;
+  plan_cache(*cfg, labels_host, P);
+  if (bytes < P.bytes) return fail(HC_ERR_SIZE, "buffer %zu < %zu bytes", bytes, P.bytes);
+  if (!P.items.empty())
+    HC_CUDA(cudaMemcpy(static_cast<char*>(buf) + P.off_items, P.items.data(),
+                       P.items.size() * sizeof(WorkItem), cudaMemcpyHostToDevice),
+            "work-list upload");
+  hc_cache* c = new hc_cache;
+  std::memset(c, 0, sizeof *c);
+  c->cfg = *cfg;
+  c->g = make_geom(*cfg);
+  std::memcpy(c->labels, labels_host, cfg->n_heads);
+  std::memcpy(c->heads, P.heads, sizeof(HeadSlot) * cfg->n_heads);
+  c->buf = static_cast<char*>(buf);
+  c->bytes = bytes;
+  c->used = P.bytes;
+  c->off_items = P.off_items;
+  c->off_k = P.off_k;
+  c->off_v = P.off_v;
+  c->n_items = (int)P.items.size();
+  c->rows = P.rows;
+  for (int a = 0; a < 4; ++a) {
+    c->rows_by_arch[a] = P.rows_by_arch[a];
+    c->n_by_arch[a] = P.n_by_arch[a];
+  }
+  c->newest = -1;
+  c->valid_frames = 0;
+  c->sink_present = false;
+  *out = c;
+  return HC_OK;
+}
+
+hc_status hc_cache_destroy(hc_cache* cache) {
+  delete cache;
+  return HC_OK;
+}
+
+hc_status hc_cache_get_info(const hc_cache* c, hc_cache_info* out) {
+  if (!c || !out) return fail(HC_ERR_INVALID_ARG, "null argument");
+  std::memset(out, 0, sizeof *out);
+  out->newest_block = c->newest;
+  out->valid_frames = c->valid_frames;
+  out->sink_present = c->sink_present ? 1 : 0;
+  for (int a = 0; a < 4; ++a) {
+    out->n_by_archetype[a] = c->n_by_arch[a];
+    out->rows_by_archetype[a] = c->rows_by_arch[a];
+  }
+  out->bytes = c->used;
+  out->monolithic_bytes = (size_t)2 * c->g.Wf * c->g.F * c->g.H * c->g.d * esize_of(c->cfg.dtype);
+  return HC_OK;
+}
+
+static hc::ScatterParams scatter_params(const hc_cache* c, const void* k, const void* v) {
+  hc::ScatterParams p;
+  std::memset(&p, 0, sizeof p);
+  p.k_src = k;
+  p.v_src = v;
+  p.k_dst = c->buf + c->off_k;
+  p.v_dst = c->buf + c->off_v;
+  p.esize = (int)esize_of(c->cfg.dtype);
+  p.g = c->g;
+  std::memcpy(p.heads, c->heads, sizeof(HeadSlot) * c->g.H);
+  return p;
+}
+
+hc_status hc_cache_restructure(hc_cache* c, const void* k_win, const void* v_win,
+                               int64_t first_block_id, int32_t n_blocks, void* stream) {
+  if (!c || !k_win || !v_win) return fail(HC_ERR_INVALID_ARG, "null argument");
+  if (!aligned16(k_win) || !aligned16(v_win)) return fail(HC_ERR_ALIGN, "k_win/v_win not 16-byte aligned");
+  const Geom& g = c->g;
+  if (first_block_id < 0 || n_blocks < 1 || (int64_t)n_blocks * g.fpb > g.Wf)
+    return fail(HC_ERR_SHAPE, "window of %d blocks from block %lld does not fit %d frames", n_blocks,
+                (long long)first_block_id, g.Wf);
+  if (first_block_id != 0 && (int64_t)n_blocks * g.fpb != g.Wf)
+    return fail(HC_ERR_STATE, "a window that does not start at block 0 must be full");
+  hc::ScatterParams p = scatter_params(c, k_win, v_win);
+  p.src_frame0 = first_block_id * g.fpb;
+  p.n_src_frames = n_blocks * g.fpb;
+  p.dummy_frame0 = (first_block_id + n_blocks - 1) * g.fpb;
+  HC_CUDA(hc::launch_scatter(p, static_cast<cudaStream_t>(stream)), "cache restructure");
+  c->newest = first_block_id + n_blocks - 1;
+  c->valid_frames = first_block_id == 0 ? n_blocks * g.fpb : g.Wf;
+  c->sink_present = c->sink_present || first_block_id == 0;
+  return HC_OK;
+}
+
+hc_status hc_cache_append(hc_cache* c, int64_t block_id, const void* k_blk, const void* v_blk,
+                          void* stream) {
+  if (!c || !k_blk || !v_blk) return fail(HC_ERR_INVALID_ARG, "null argument");
+  if (!aligned16(k_blk) || !aligned16(v_blk)) return fail(HC_ERR_ALIGN, "k_blk/v_blk not 16-byte aligned");
+  if (c->newest < 0 ? block_id != 0 : (block_id != c->newest && block_id != c->newest + 1))
+    return fail(HC_ERR_STATE, "block %lld after newest %lld: must repeat it or follow it",
+                (long long)block_id, (long long)c->newest);
+  const Geom& g = c->g;
+  hc::ScatterParams p = scatter_params(c, k_blk, v_blk);
+  p.src_frame0 = block_id * g.fpb;
+  p.n_src_frames = g.fpb;
+  p.dummy_frame0 = block_id * g.fpb;
+  HC_CUDA(hc::launch_scatter(p, static_cast<cudaStream_t>(stream)), "cache append");
+  c->newest = block_id;
+  const int64_t seen = (block_id + 1) * g.fpb;
+  c->valid_frames = std::max<int64_t>(c->valid_frames, std::min<int64_t>(seen, g.Wf));
+  if (block_id == 0) c->sink_present = true;
+  return HC_OK;
+}
+
+// ------------------------------------------------------------ attention
+
+hc_status hc_routed_attention(const hc_cache* c, const void* q, void* o, void* stream) {
+  if (!c || !q || !o) return fail(HC_ERR_INVALID_ARG, "null argument");
+  if (!aligned16(q) || !aligned16(o)) return fail(HC_ERR_ALIGN, "q/o not 16-byte aligned");
+  if (c->newest < 0) return fail(HC_ERR_STATE, "cache holds no block yet");
+  if (c->n_by_arch[HC_SINK] > 0 && !c->sink_present)
+    return fail(HC_ERR_STATE, "Sink heads present but block 0 was never written");
+  int* status = nullptr;
+  hc_status s = status_ptr(&status);
+  if (s != HC_OK) return s;
+  hc::AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q;
+  p.k = c->buf + c->off_k;
+  p.v = c->buf + c->off_v;
+  p.o = o;
+  p.k_stride = c->g.d;
+  p.k_hstride = 0;
+  p.nq_total = c->g.blk;
+  p.out_fp32 = c->cfg.dtype == HC_FP32;
+  p.item_mode = hc::ITEMS_LIST;
+  p.n_items = c->n_items;
+  p.items = reinterpret_cast<const WorkItem*>(c->buf + c->off_items);
+  p.valid_frames = c->valid_frames;
+  p.g = c->g;
+  p.status = status;
+  HC_CUDA(hc::launch_attention(p, c->cfg.dtype, dim3(c->n_items, 1, 1), static_cast<cudaStream_t>(stream)),
+          "routed attention");
+  return HC_OK;
+}
+
+hc_status hc_full_attention(const hc_config* cfg, const void* q, const void* k, const void* v,
+                            int32_t n_q_tokens, int32_t n_key_frames, void* o, void* stream) {
+  hc_status s = hc_config_validate(cfg);
+  if (s != HC_OK) return s;
+  if (!q || !k || !v || !o) return fail(HC_ERR_INVALID_ARG, "null argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(HC_ERR_ALIGN, "device pointers must be 16-byte aligned");
+  if (n_q_tokens < 0 || n_key_frames < 1 || n_key_frames > 4096)
+    return fail(HC_ERR_SHAPE, "n_q_tokens %d / n_key_frames %d", n_q_tokens, n_key_frames);
+  const Geom g = make_geom(*cfg);
+  const int64_t nk = (int64_t)n_key_frames * g.F;
+  if (nk >= (1ll << 31)) return fail(HC_ERR_SHAPE, "too many keys");
+  int* status = nullptr;
+  if ((s = status_ptr(&status)) != HC_OK) return s;
+  const int BM = hc::attention_block_rows(cfg->dtype, cfg->head_dim);
+  hc::AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.k_stride = (int64_t)g.H * g.d;
+  p.k_hstride = g.d;
+  p.nq_total = n_q_tokens;
+  p.out_fp32 = cfg->dtype == HC_FP32;
+  p.item_mode = hc::ITEMS_DENSE;
+  p.plane_k0[0] = 0;
+  p.plane_klen[0] = (int32_t)nk;
+  p.g = g;
+  p.status = status;
+  HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3((n_q_tokens + BM - 1) / BM, g.H, 1),
+                               static_cast<cudaStream_t>(stream)),
+          "full attention");
+  return HC_OK;
+}
+
+hc_status hc_get_last_error(void* stream) {
+  HC_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize");
+  int word = 0, zero = 0;
+  HC_CUDA(cudaMemcpyFromSymbol(&word, g_hc_status_word, sizeof word), "status read");
+  HC_CUDA(cudaMemcpyToSymbol(g_hc_status_word, &zero, sizeof zero), "status clear");
+  if (word == hc::DEV_OK) return HC_OK;
+  if (word == hc::DEV_TIMEOUT) return fail(HC_ERR_TIMEOUT, "a bounded device wait expired");
+  return fail(HC_ERR_CUDA, "device status word %d", word);
+}
+
+}  // extern "C"

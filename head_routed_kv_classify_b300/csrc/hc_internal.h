@@ -1,0 +1,140 @@
+// Internal declarations shared by the library's translation units.
+//
+// Geometry, work items and the cell arithmetic of the deployed Spatial path
+// (non-overlapping cells of cell_h x cell_w tokens, the last cell along an
+// axis taking the rounded remainder: n_cells = max(1, floor(N/c + 1/2))).
+// [Pith review of HeadCast, Ledger "deployed spatial grid cell = 10x10 with
+//  rounded remainder"; major comment 2; Figure 3 caption.]
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/headcast.h"
+
+namespace hc {
+
+#define HC_HD __host__ __device__ __forceinline__
+
+// Layer geometry as the kernels see it.
+struct Geom {
+  int H, d, Fh, Fw, F, fpb, Wf, blk;   // blk = fpb * F (tokens per block)
+  int cell_h, cell_w, ncell_h, ncell_w;
+  int radius;
+  float scale_log2;                    // softmax scale * log2(e)
+};
+
+HC_HD int n_cells(int n, int c) {            // max(1, floor(n/c + 1/2))
+  int k = (2 * n + c) / (2 * c);
+  return k < 1 ? 1 : k;
+}
+HC_HD int cell_index(int x, int c, int nc) {
+  int i = x / c;
+  return i < nc - 1 ? i : nc - 1;
+}
+HC_HD int cell_extent(int i, int n, int c, int nc) {
+  return i < nc - 1 ? c : n - (nc - 1) * c;
+}
+// Tokens of one frame that precede cell (ci, cj) in cell-major order.  Every
+// cell row above ci is cell_h tall; cells left of cj in row ci are cell_w
+// wide and share row ci's height.
+HC_HD int cell_tokens_before(const Geom& g, int ci, int cj) {
+  int hz = cell_extent(ci, g.Fh, g.cell_h, g.ncell_h);
+  return ci * g.cell_h * g.Fw + hz * cj * g.cell_w;
+}
+
+// Work item kinds.
+enum : int32_t {
+  ITEM_RANGE = 0,   // queries q0.. (block-local tokens), keys: one run of rows
+  ITEM_CELL = 1,    // queries: ordinals q0.. of one cell's 3-frame query set
+  ITEM_PROXY = 2,   // queries q0.. inside one frame; keys: (2r+1) neighbourhood rows of every frame
+};
+
+struct alignas(16) WorkItem {
+  int32_t head;
+  int32_t kind;
+  int32_t q0;
+  int32_t nq;
+  int64_t k_row0;       // first key row in the key buffer's row space
+  int32_t k_len;        // keys when k_per_frame == 0
+  int32_t k_per_frame;  // > 0: k_len = k_per_frame * valid_frames
+  int32_t cell;         // ITEM_CELL: ci * ncell_w + cj
+  int32_t out_plane;
+  int32_t pad0, pad1;
+};
+static_assert(sizeof(WorkItem) == 48, "WorkItem layout");
+
+// Item source for an attention launch.
+enum : int32_t {
+  ITEMS_LIST = 0,     // items[blockIdx.x]
+  ITEMS_DENSE = 1,    // x: q tile, y: head, z: plane -> RANGE over plane_k0/plane_klen
+  ITEMS_PROXY = 2,    // x: frame * tiles_per_frame + t, y: head -> PROXY
+};
+
+struct AttnParams {
+  const void* q;            // [Nq][H][d]
+  const void* k;            // key buffer base
+  const void* v;            // value buffer base
+  void* o;                  // output base (plane 0)
+  int64_t k_stride;         // elements between consecutive key rows
+  int64_t k_hstride;        // elements between heads inside a key row (0 for per-head buffers)
+  int64_t o_plane_stride;   // elements between output planes
+  int32_t nq_total;         // queries in the block (3F or caller's Nq)
+  int32_t out_fp32;         // 1: fp32 output, 0: input dtype
+  int32_t item_mode;
+  int32_t n_items;
+  const WorkItem* items;
+  int32_t valid_frames;
+  int32_t proxy_frames;     // frames of keys for ITEMS_PROXY
+  int32_t tiles_per_frame;  // ITEMS_PROXY q tiles per frame
+  int32_t pad;
+  int64_t plane_k0[4];
+  int32_t plane_klen[4];
+  Geom g;
+  int* status;
+};
+
+// Status codes a kernel may write to the device status word.
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 7, DEV_BOUNDS = 6 };
+
+// Launchers (attn.cu).
+cudaError_t launch_attention(const AttnParams& p, int dtype, dim3 grid, cudaStream_t s);
+int attention_block_rows(int dtype, int d);   // queries per item tile
+
+// Classification post-processing (classify.cu).
+struct ClassifyPost {
+  const float* planes;      // 4 planes fp32 [Nq][H][d]: full, sink, dummy, proxy
+  int64_t plane_stride;
+  float* tok;               // [4][H][Nq]: cos_sink, cos_dummy, cos_spatial, sqerr
+  void* o_full;             // nullable, dtype of the inputs
+  int32_t o_full_fp32;
+  int8_t* labels;
+  float* stats;             // nullable [H][6]
+  int32_t nq;
+  Geom g;
+  float theta_sink, theta_dummy, theta_spatial, theta_score, gamma;
+};
+cudaError_t launch_classify_post(const ClassifyPost& c, cudaStream_t s);
+
+// Cache scatter (cache.cu).
+struct HeadSlot {
+  int32_t arch;
+  int32_t pad;
+  int64_t row0;
+};
+struct ScatterParams {
+  const void* k_src;        // [n_src_frames*F][H][d]
+  const void* v_src;
+  void* k_dst;              // K area [rows][d]
+  void* v_dst;              // V area [rows][d]
+  int64_t src_frame0;       // absolute index of the first source frame
+  int32_t n_src_frames;
+  int32_t esize;            // bytes per element
+  int64_t dummy_frame0;     // absolute first frame of the newest block (Dummy target)
+  Geom g;
+  HeadSlot heads[HC_MAX_HEADS];
+};
+cudaError_t launch_scatter(const ScatterParams& p, cudaStream_t s);
+
+}  // namespace hc

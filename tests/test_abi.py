@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, and its host-only calls (config, validation, cache sizing)
+behave as documented."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import head_routed_kv_classify_b300 as hc
+from head_routed_kv_classify_b300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "headcast.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return hc.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hc_[a-z_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(hc.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", hc.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_library_does_not_need_libcuda(lib):
+    out = subprocess.run(["ldd", hc.LIB_PATH], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out and "libcudart.so" not in out
+
+
+def test_abi_version_and_strings(lib):
+    assert lib.hc_abi_version() == 1
+    assert lib.hc_status_string(0) == b"ok"
+    assert lib.hc_status_string(7) == b"device-side wait expired"
+
+
+def test_config_default_holds_ledger_constants(lib):
+    cfg = hc.hc_config_default()
+    assert abs(cfg.theta_sink - 0.95) < 1e-7 and abs(cfg.theta_dummy - 0.95) < 1e-7
+    assert abs(cfg.theta_spatial - 0.95) < 1e-7 and abs(cfg.theta_score - 0.755) < 1e-7
+    assert cfg.gamma == 5.0 and cfg.proxy_radius == 2 and (cfg.cell_h, cfg.cell_w) == (10, 10)
+    assert cfg.frames_per_block == 3 and cfg.window_frames == 21
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("n_heads", 0, "HC_ERR_SHAPE"), ("n_heads", 65, "HC_ERR_SHAPE"),
+    ("head_dim", 96, "HC_ERR_SHAPE"), ("frame_h", 0, "HC_ERR_SHAPE"),
+    ("window_frames", 20, "HC_ERR_SHAPE"), ("dtype", 7, "HC_ERR_DTYPE"),
+    ("theta_sink", float("nan"), "HC_ERR_INVALID_ARG"), ("softmax_scale", -1.0, "HC_ERR_INVALID_ARG"),
+    ("cell_w", 0, "HC_ERR_INVALID_ARG"), ("proxy_radius", -1, "HC_ERR_INVALID_ARG"),
+])
+def test_config_validation(lib, field, value, status):
+    cfg = hc.make_config(12, 128, 45, 80)
+    hc.hc_config_validate(cfg)
+    setattr(cfg, field, value)
+    with pytest.raises(hc.HeadcastError) as e:
+        hc.hc_config_validate(cfg)
+    assert e.value.name == status
+    assert lib.hc_last_error_message() != b""
+
+
+def test_cache_bytes_720p(lib):
+    cfg = hc.make_config(12, 128, 45, 80)
+    labels = [0, 0, 1, 1, 1, 2, 2, 2, 2, 3, 3, 3]
+    n = hc.hc_cache_bytes(cfg, labels)
+    F, d = 3600, 128
+    rows = 5 * 3 * F + 7 * 21 * F
+    assert n >= 2 * rows * d * 2
+    assert n < 2 * rows * d * 2 + 2 * 1024 * 1024      # work list + alignment
+    mono = 2 * 21 * F * 12 * d * 2
+    assert n < 0.66 * mono
+
+
+def test_cache_bytes_rejects_bad_labels(lib):
+    cfg = hc.make_config(4, 64, 8, 8, 12)
+    with pytest.raises(hc.HeadcastError) as e:
+        hc.hc_cache_bytes(cfg, [0, 1, 2, 4])
+    assert e.value.name == "HC_ERR_INVALID_ARG"
+
+
+def test_null_arguments_rejected_before_any_cuda_call(lib):
+    cfg = hc.make_config(4, 64, 8, 8, 12)
+    n = C.c_size_t(0)
+    assert lib.hc_classify(C.byref(cfg), None, None, None, 12, None, None, None, None, None, 0,
+                           None) == 1
+    assert lib.hc_cache_bytes(C.byref(cfg), None, C.byref(n)) == 1
+    assert lib.hc_routed_attention(None, None, None, None) == 1
+    assert lib.hc_full_attention(C.byref(cfg), None, None, None, 192, 12, None, None) == 1
+
+
+def test_misaligned_pointers_rejected(lib):
+    cfg = hc.make_config(4, 64, 8, 8, 12)
+    p = C.c_void_p(0x1008)
+    lab = np.zeros(4, np.int8)
+    st = lib.hc_classify(C.byref(cfg), p, p, p, 12, C.c_void_p(0x2000), None, None, None,
+                         C.c_void_p(0x3000), 1 << 30, None)
+    assert st == 4
+    assert lib.hc_full_attention(C.byref(cfg), p, p, p, 192, 12, p, None) == 4
+    handle = C.c_void_p(0)
+    assert lib.hc_cache_create(C.byref(cfg), lab.ctypes.data_as(C.c_void_p), C.c_void_p(0x1010),
+                               1 << 30, C.byref(handle)) == 4
+
+
+def test_classify_rejects_short_window_and_small_scratch(lib):
+    cfg = hc.make_config(4, 64, 8, 8, 12)
+    p = C.c_void_p(0x10000)
+    assert lib.hc_classify(C.byref(cfg), p, p, p, 3, p, None, None, None, p, 1 << 30, None) == 2
+    assert lib.hc_classify(C.byref(cfg), p, p, p, 12, p, None, None, None, p, 16, None) == 9

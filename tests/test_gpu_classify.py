@@ -1,0 +1,104 @@
+"""GPU parity of the one-time head classification: labels bit-exact against
+the oracle (and the planted archetypes), per-head statistics and the
+full-context output against the oracle's."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import headcast_ref as ref
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+hc = pytest.importorskip("head_routed_kv_classify_b300")
+
+SMALL = {
+    "tiny": synth.SHAPES["tiny"],
+    "tiny_bf16": synth.custom_shape("tiny_bf16", n_heads=4, head_dim=64, frame_h=8, frame_w=8,
+                                    window_frames=12, dtype="bf16", seed=10),
+    "ragged": synth.custom_shape("ragged", n_heads=8, head_dim=64, frame_h=23, frame_w=27,
+                                 window_frames=12, dtype="bf16", seed=11),
+    "ragged_d128": synth.custom_shape("ragged_d128", n_heads=4, head_dim=128, frame_h=13,
+                                      frame_w=17, window_frames=9, dtype="bf16", seed=12,
+                                      mix=(3, 2, 1, 0)),
+}
+
+# Statistics tolerances (fp32 per-token values from bf16-probability outputs
+# versus fp64): mean cosines and P5 to 2e-3, MSE to 5% + 1e-5.
+STAT_ATOL = 2e-3
+
+
+def _run(shape, o_full=True):
+    cfg = hc.config_for(shape)
+    inp = synth.make_layer(shape)
+    q, k, v = (gu.to_dev(x, shape.dtype) for x in (inp.q, inp.k, inp.v))
+    of = gu.torch().empty_like(q) if o_full else None
+    labels, _, stats = hc.hc_classify(cfg, q, k, v, o_full=of)
+    hc.hc_get_last_error()
+    return inp, labels, gu.to_host(stats), (gu.to_host(of) if o_full else None)
+
+
+def _compare_stats(got, want, what):
+    for h in range(want.shape[0]):
+        for j in (0, 1, 2, 3, 5):
+            assert abs(got[h, j] - want[h, j]) <= STAT_ATOL, (what, h, j, got[h], want[h])
+        assert abs(got[h, 4] - want[h, 4]) <= 0.05 * abs(want[h, 4]) + 1e-5, (what, h, got[h], want[h])
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_classify_small(name):
+    shape = SMALL[name]
+    inp, labels, stats, of = _run(shape)
+    geom = ref.geometry_of(shape)
+    cls = ref.classify(inp.q.values, inp.k.values, inp.v.values, geom)
+    assert list(labels) == list(cls.labels), (labels, cls.labels, cls.margins)
+    assert list(labels) == list(inp.planted)
+    _compare_stats(stats, cls.stats, name)
+    want_full = np.stack([o.o_full for o in cls.outputs], axis=1)
+    gu.assert_close(of, want_full, shape.dtype, f"{name} o_full")
+
+
+def test_classify_480p():
+    shape = synth.SHAPES["480p"]
+    inp, labels, stats, of = _run(shape)
+    cls = ref.classify(inp.q.values, inp.k.values, inp.v.values, ref.geometry_of(shape))
+    assert list(labels) == list(cls.labels) == list(inp.planted), cls.margins
+    _compare_stats(stats, cls.stats, "480p")
+    want_full = np.stack([o.o_full for o in cls.outputs], axis=1)
+    gu.assert_close(of, want_full, "bf16", "480p o_full")
+
+
+@pytest.mark.parametrize("name", ["720p", "1080p"])
+def test_classify_full_size_planted(name):
+    """At full size the oracle's per-head means need every query, so labels
+    are checked against the planted archetypes (with >= 0.02 margins on the
+    GPU's own statistics) and the full-context output on sampled queries."""
+    shape = synth.SHAPES[name]
+    inp, labels, stats, of = _run(shape)
+    assert list(labels) == list(inp.planted), (labels, stats)
+    th = ref.Thresholds()
+    for h in range(shape.n_heads):
+        m = ref.margins(stats[h], th)
+        lab = labels[h]
+        gates = {0: [0], 1: [0, 1], 2: [0, 1, 2, 3], 3: [0, 1]}[int(lab)]
+        assert all(abs(m[g]) >= 0.02 for g in gates), (h, m)
+    idx = gu.sample_queries(shape.n_q, 12, seed=shape.seed + 7)
+    geom = ref.geometry_of(shape)
+    for h in (0, 5, 9):
+        o = ref.classification_outputs(inp.q.values, inp.k.values, inp.v.values, geom, h,
+                                       query_idx=idx)
+        gu.assert_close(of[idx, h], o.o_full, "bf16", f"{name} o_full head {h}")
+
+
+def test_classify_thresholds_are_read_from_config():
+    """Raising theta above every head's similarity turns every head Global;
+    lowering theta_sink below every c_sink turns every head Sink."""
+    shape = SMALL["tiny_bf16"]
+    inp = synth.make_layer(shape)
+    q, k, v = (gu.to_dev(x, "bf16") for x in (inp.q, inp.k, inp.v))
+    cfg = hc.config_for(shape, theta_sink=1.5, theta_dummy=1.5, theta_spatial=1.5)
+    labels, _, _ = hc.hc_classify(cfg, q, k, v)
+    assert list(labels) == [3, 3, 3, 3]
+    cfg = hc.config_for(shape, theta_sink=-1.5)
+    labels, _, _ = hc.hc_classify(cfg, q, k, v)
+    assert list(labels) == [0, 0, 0, 0]
