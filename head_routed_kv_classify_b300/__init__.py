@@ -10,7 +10,7 @@ Names mirror the C ABI in include/headcast.h:
     hc_config_default, hc_config_validate, hc_classify_scratch_bytes,
     hc_classify, hc_cache_bytes, hc_cache_create (-> Cache),
     hc_cache_restructure, hc_cache_append, hc_routed_attention,
-    hc_full_attention, hc_get_last_error
+    hc_full_attention, hc_get_last_error, hc_classify_static_scratch
 """
 from __future__ import annotations
 
@@ -29,12 +29,14 @@ STATUS_NAMES = {0: "HC_OK", 1: "HC_ERR_INVALID_ARG", 2: "HC_ERR_SHAPE", 3: "HC_E
                 4: "HC_ERR_ALIGN", 5: "HC_ERR_STATE", 6: "HC_ERR_CUDA", 7: "HC_ERR_TIMEOUT",
                 8: "HC_ERR_UNSUPPORTED", 9: "HC_ERR_SIZE"}
 MAX_HEADS = 64
+STATIC_SCRATCH_BYTES = 16 << 20   # HC_STATIC_SCRATCH_BYTES
 
 # Every symbol include/headcast.h declares.
 EXPORTS = ("hc_abi_version", "hc_status_string", "hc_last_error_message", "hc_config_default",
            "hc_config_validate", "hc_classify_scratch_bytes", "hc_classify", "hc_cache_bytes",
            "hc_cache_create", "hc_cache_destroy", "hc_cache_get_info", "hc_cache_restructure",
-           "hc_cache_append", "hc_routed_attention", "hc_full_attention", "hc_get_last_error")
+           "hc_cache_append", "hc_routed_attention", "hc_full_attention", "hc_get_last_error",
+           "hc_classify_static_scratch")
 
 
 class HeadcastUnavailable(RuntimeError):
@@ -102,6 +104,7 @@ def load(path: str = LIB_PATH):
         "hc_routed_attention": (C.c_int, [vp, vp, vp, vp]),
         "hc_full_attention": (C.c_int, [cfgp, vp, vp, vp, i32, i32, vp, vp]),
         "hc_get_last_error": (C.c_int, [vp]),
+        "hc_classify_static_scratch": (C.c_int, [cfgp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -212,6 +215,31 @@ def hc_classify(cfg, q, k, v, n_key_frames=None, labels_dev=None, stats_dev=None
         host.ctypes.data_as(C.c_void_p) if host is not None else None,
         _ptr(stats_dev, None, "stats_dev"), _ptr(o_full, cfg, "o_full"),
         _ptr(scratch, None, "scratch"), scratch.numel() * scratch.element_size(), _stream(stream)))
+    return host, labels_dev, stats_dev
+
+
+def hc_classify_static_scratch(cfg, q, k, v, n_key_frames=None, labels_dev=None, stats_dev=None,
+                               o_full=None, stream=None, copy_labels=True):
+    """hc_classify for callers that cannot allocate device memory: the
+    library supplies the workspace from a fixed device array (at most
+    STATIC_SCRATCH_BYTES).  labels_dev and stats_dev must then be passed in
+    by such a caller; they are only created here when omitted.  Returns
+    (labels_host int8[H] or None, labels_dev, stats_dev)."""
+    t = _torch()
+    nkf = cfg.window_frames if n_key_frames is None else n_key_frames
+    H, d = cfg.n_heads, cfg.head_dim
+    dev = q.device
+    if labels_dev is None:
+        labels_dev = t.empty(H, dtype=t.int8, device=dev)
+    if stats_dev is None:
+        stats_dev = t.empty((H, 6), dtype=t.float32, device=dev)
+    host = np.zeros(H, dtype=np.int8) if copy_labels else None
+    _check(load().hc_classify_static_scratch(
+        C.byref(cfg), _ptr(q, cfg, "q", (cfg.block_tokens, H, d)),
+        _ptr(k, cfg, "k", (nkf * cfg.F, H, d)), _ptr(v, cfg, "v", (nkf * cfg.F, H, d)), nkf,
+        _ptr(labels_dev, None, "labels_dev"),
+        host.ctypes.data_as(C.c_void_p) if host is not None else None,
+        _ptr(stats_dev, None, "stats_dev"), _ptr(o_full, cfg, "o_full"), _stream(stream)))
     return host, labels_dev, stats_dev
 
 

@@ -190,6 +190,16 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
 
 }  // namespace
 
+hc_status hc::record_error(hc_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return s;
+}
+
 // ===========================================================================
 
 extern "C" {

@@ -95,6 +95,9 @@ struct AttnParams {
   int* status;
 };
 
+// Record a failure message for hc_last_error_message and return `s`.
+hc_status record_error(hc_status s, const char* fmt, ...);
+
 // Status codes a kernel may write to the device status word.
 enum : int { DEV_OK = 0, DEV_TIMEOUT = 7, DEV_BOUNDS = 6 };
 

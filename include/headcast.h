@@ -160,6 +160,32 @@ hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const 
                       void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Classification with a library-held workspace.  The paper has no
+ * counterpart to this call: it exists for callers that cannot allocate
+ * device memory (for instance a plugin whose host framework owns all device
+ * memory, or a real-time loop that allows no allocation after start-up).
+ * It computes exactly what hc_classify computes, with the same arguments
+ * except the workspace, which here is a fixed array of
+ * HC_STATIC_SCRATCH_BYTES in the library's device image.  Every GPU that
+ * loads the library holds that array until the process exits.  The call
+ * itself allocates nothing (no cudaMalloc, no allocating library routine).
+ *  - HC_ERR_SIZE if the layer's workspace (hc_classify_scratch_bytes) is
+ *    larger than HC_STATIC_SCRATCH_BYTES; nothing is launched.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the array and it keeps the last call's contents
+ *    (nothing in it needs clearing between calls).  Calls whose kernels may
+ *    overlap on the GPU (different streams or threads) race on it and must
+ *    be serialised by the caller.
+ * ------------------------------------------------------------------------- */
+#define HC_STATIC_SCRATCH_BYTES (16u << 20)
+hc_status hc_classify_static_scratch(const hc_config* cfg, const void* q, const void* k,
+                                     const void* v, int32_t n_key_frames, int8_t* labels_dev,
+                                     int8_t* labels_host, float* stats_dev, void* o_full,
+                                     void* stream);
+
+/* ---------------------------------------------------------------------------
  * Restructured cache.  The monolithic [window][H][d] K/V cache is replaced
  * by per-head regions in one caller-owned device buffer:
  *   Sink head     one block (3F rows): block 0 of the stream, fixed;
