@@ -335,11 +335,17 @@ hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const 
   p.plane_klen[2] = g.blk;
   p.g = g;
   p.status = status;
-  HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3((g.blk + BM - 1) / BM, g.H, 3), st),
-          "classification attention");
+  if (cfg->dtype == HC_BF16) {
+    const hc::TcKV kv{k, v, g.H, nk};
+    HC_CUDA(hc::launch_attention_tc(p, kv, dim3((g.blk + BM - 1) / BM, g.H, 3), st), "classification attention");
+  } else {
+    HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3((g.blk + BM - 1) / BM, g.H, 3), st),
+            "classification attention");
+  }
+  const int PBM = hc::proxy_block_rows();
   p.item_mode = hc::ITEMS_PROXY;
   p.proxy_frames = n_key_frames;
-  p.tiles_per_frame = (g.F + BM - 1) / BM;
+  p.tiles_per_frame = (g.F + PBM - 1) / PBM;
   HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3(g.fpb * p.tiles_per_frame, g.H, 1), st),
           "classification proxy attention");
 
@@ -520,8 +526,14 @@ hc_status hc_routed_attention(const hc_cache* c, const void* q, void* o, void* s
   p.valid_frames = c->valid_frames;
   p.g = c->g;
   p.status = status;
-  HC_CUDA(hc::launch_attention(p, c->cfg.dtype, dim3(c->n_items, 1, 1), static_cast<cudaStream_t>(stream)),
-          "routed attention");
+  if (c->cfg.dtype == HC_BF16) {
+    const hc::TcKV kv{c->buf + c->off_k, c->buf + c->off_v, 1, c->rows};
+    HC_CUDA(hc::launch_attention_tc(p, kv, dim3(c->n_items, 1, 1), static_cast<cudaStream_t>(stream)),
+            "routed attention");
+  } else {
+    HC_CUDA(hc::launch_attention(p, c->cfg.dtype, dim3(c->n_items, 1, 1), static_cast<cudaStream_t>(stream)),
+            "routed attention");
+  }
   return HC_OK;
 }
 
@@ -555,9 +567,13 @@ hc_status hc_full_attention(const hc_config* cfg, const void* q, const void* k, 
   p.plane_klen[0] = (int32_t)nk;
   p.g = g;
   p.status = status;
-  HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3((n_q_tokens + BM - 1) / BM, g.H, 1),
-                               static_cast<cudaStream_t>(stream)),
-          "full attention");
+  const dim3 grid((n_q_tokens + BM - 1) / BM, g.H, 1);
+  if (cfg->dtype == HC_BF16) {
+    const hc::TcKV kv{k, v, g.H, nk};
+    HC_CUDA(hc::launch_attention_tc(p, kv, grid, static_cast<cudaStream_t>(stream)), "full attention");
+  } else {
+    HC_CUDA(hc::launch_attention(p, cfg->dtype, grid, static_cast<cudaStream_t>(stream)), "full attention");
+  }
   return HC_OK;
 }
 

@@ -445,7 +445,8 @@ cudaError_t launch_bf16(const AttnParams& p, dim3 grid, cudaStream_t s) {
 
 }  // namespace
 
-int attention_block_rows(int, int) { return kBM; }
+int attention_block_rows(int dtype, int) { return dtype == HC_BF16 ? tc_block_rows() : kBM; }
+int proxy_block_rows() { return kBM; }
 
 cudaError_t launch_attention(const AttnParams& p, int dtype, dim3 grid, cudaStream_t s) {
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;

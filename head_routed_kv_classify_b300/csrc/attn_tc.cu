@@ -1,0 +1,608 @@
+// Softmax attention on the 5th-generation tensor cores (tcgen05 + TMEM),
+// with K/V tiles streamed by TMA.  Serves every bf16 attention of the
+// library: the routed pathways (Sink / Dummy / Global key runs and Spatial
+// cells of the restructured cache), the in-house full attention and the
+// full / Sink / Dummy planes of classification.
+// [Pith review of HeadCast: "The pith" and "Core claim" (each head attends
+//  only over its pathway), "What carries the argument" (the classification
+//  outputs), major comment 2 and Figure 3 caption (10x10 cells).]
+//
+// One CTA computes one work item: up to 128 queries of one head against one
+// contiguous run of key rows.  Roles (192 threads):
+//   warps 0-3  softmax: thread i owns query row i, i.e. TMEM lane i.  It
+//              reads its row of S = Q K^T from TMEM, keeps the running max
+//              and sum, writes P (bf16) to shared memory and, when the max
+//              has grown by more than 2^8, rescales its row of O in TMEM;
+//              at the end it normalises O and stores it.
+//   warp 4     TMA producer: K and V tiles of 128 keys into a 2-stage ring.
+//   warp 5     MMA issuer: S(j) = Q K(j)^T into one of two S buffers in
+//              TMEM, O += P(j) V(j) into the O accumulator in TMEM.
+// Hand-offs are mbarriers; every wait is bounded in wall-clock time and on
+// expiry the CTA records HC_ERR_TIMEOUT in the status word, drains its own
+// copies and MMAs (again bounded), frees TMEM and returns.
+//
+// Shared-memory operand layouts are the canonical 128-byte-swizzle ones:
+// Q, K and P are K-major (rows of 64 bf16 = 128 B, 8-row atoms of 1 KB,
+// one region per 64 columns); V is the MN-major B operand of P V (rows are
+// keys, 128 B per 64 channels of d).
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "hc_internal.h"
+
+namespace hc {
+namespace {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int BM = 128;            // queries per item (one MMA M)
+constexpr int BN = 128;            // keys per tile
+constexpr int STAGES = 2;          // K/V ring depth
+constexpr int NTHREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float RESCALE_LOG2 = 8.f;  // rescale O when the row max grows by > 2^8
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;   // 1 s
+constexpr unsigned long long DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s
+
+template <int D>
+struct Layout {
+  static constexpr int NREG = D / 64;               // 64-column regions along d
+  static constexpr int Q_REG = BM * 128;
+  static constexpr int KV_REG = BN * 128;
+  static constexpr int KV_BYTES = NREG * KV_REG;    // one K (or V) tile
+  static constexpr int P_REG = BM * 128;
+  static constexpr int P_BYTES = (BN / 64) * P_REG;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + NREG * Q_REG;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int BYTES = OFF_BAR + 256;
+  static constexpr int ALLOC = BYTES + 1024;        // room to align the base to 1 KB
+  static constexpr uint32_t COL_O = 2 * BN;         // TMEM: S0 [0,BN), S1 [BN,2BN), O [2BN, 2BN+D)
+};
+
+// Barrier slots (8 bytes each) after OFF_BAR.
+enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_SFULL = 8, B_PFULL = 10,
+       B_PVDONE = 12, B_FIN = 14, B_COUNT = 15 };
+
+struct TcArgs {
+  CUtensorMap tk;        // K as [rows][heads][D] (3-D map, box {64, 1, BN})
+  CUtensorMap tv;        // V, same shape
+  AttnParams p;
+  int32_t kv_head_coord; // 1: the map's middle coordinate is the head; 0: always 0
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until phase `parity` of `bar` has completed, for at most `limit` ns
+// or until another role has raised the CTA's abort flag.
+__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               unsigned long long limit) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (now_ns() - t0 > limit) return false;
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 form): start address, leading and
+// stride byte offsets (all >> 4), fixed version bits 46..48 = 0b001, and the
+// 128-byte swizzle mode (2) in bits 61..63.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
+// A K-major, B K-major or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+#define HC_R32(i) "=r"(r[i])
+#define HC_R32_8(b) HC_R32(b), HC_R32(b + 1), HC_R32(b + 2), HC_R32(b + 3), HC_R32(b + 4), HC_R32(b + 5), \
+                    HC_R32(b + 6), HC_R32(b + 7)
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : HC_R32_8(0), HC_R32_8(8), HC_R32_8(16), HC_R32_8(24)
+      : "r"(taddr));
+}
+#undef HC_R32
+#define HC_W32(i) "r"(r[i])
+#define HC_W32_8(b) HC_W32(b), HC_W32(b + 1), HC_W32(b + 2), HC_W32(b + 3), HC_W32(b + 4), HC_W32(b + 5), \
+                    HC_W32(b + 6), HC_W32(b + 7)
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), HC_W32_8(0), HC_W32_8(8), HC_W32_8(16), HC_W32_8(24)
+      : "memory");
+}
+#undef HC_W32
+#undef HC_R32_8
+#undef HC_W32_8
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------- work items
+
+struct TcItem {
+  int head, kind, q0, nq, out_plane;
+  int64_t k_row0;
+  int k_len;
+  int h0, w0, hz, wz;   // ITEM_CELL: the cell
+};
+
+__device__ __forceinline__ TcItem tc_decode(const AttnParams& p) {
+  const Geom& g = p.g;
+  TcItem it;
+  it.h0 = it.w0 = it.hz = it.wz = 0;
+  if (p.item_mode == ITEMS_LIST) {
+    const WorkItem w = p.items[blockIdx.x];
+    it.head = w.head;
+    it.kind = w.kind;
+    it.q0 = w.q0;
+    it.nq = w.nq;
+    it.out_plane = w.out_plane;
+    it.k_row0 = w.k_row0;
+    it.k_len = w.k_per_frame > 0 ? w.k_per_frame * p.valid_frames : w.k_len;
+    if (w.kind == ITEM_CELL) {
+      const int ci = w.cell / g.ncell_w, cj = w.cell % g.ncell_w;
+      it.h0 = ci * g.cell_h;
+      it.hz = cell_extent(ci, g.Fh, g.cell_h, g.ncell_h);
+      it.w0 = cj * g.cell_w;
+      it.wz = cell_extent(cj, g.Fw, g.cell_w, g.ncell_w);
+    }
+  } else {  // ITEMS_DENSE
+    it.head = blockIdx.y;
+    it.kind = ITEM_RANGE;
+    it.q0 = blockIdx.x * BM;
+    it.nq = min(BM, p.nq_total - it.q0);
+    it.out_plane = blockIdx.z;
+    it.k_row0 = p.plane_k0[blockIdx.z];
+    it.k_len = p.plane_klen[blockIdx.z];
+  }
+  return it;
+}
+
+// Block-local token of the r-th query of an item.
+__device__ __forceinline__ int tc_query_token(const TcItem& it, const Geom& g, int r) {
+  if (it.kind != ITEM_CELL) return it.q0 + r;
+  const int ord = it.q0 + r;
+  const int csz = it.hz * it.wz;
+  const int fq = ord / csz, rem = ord - fq * csz;
+  const int hh = rem / it.wz, ww = rem - hh * it.wz;
+  return fq * g.F + (it.h0 + hh) * g.Fw + it.w0 + ww;
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ TcArgs args) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t sQ = s_base + L::OFF_Q, sK = s_base + L::OFF_K, sV = s_base + L::OFF_V, sP = s_base + L::OFF_P;
+  const uint32_t bars = s_base + L::OFF_BAR;
+  auto bar = [&](int slot) { return bars + 8u * slot; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 8 * B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 * B_COUNT + 4);
+
+  volatile int* skip_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 * B_COUNT + 8);
+
+  const AttnParams& p = args.p;
+  const Geom& g = p.g;
+  // Once any CTA has recorded an expired wait, the rest of the launch (and
+  // later launches, until the status word is read and cleared) skip their
+  // work so that a broken pipeline fails fast.
+  if (threadIdx.x == 0) *skip_flag = p.status ? *reinterpret_cast<volatile int*>(p.status) : 0;
+  __syncthreads();
+  if (*skip_flag) return;
+  const TcItem it = tc_decode(p);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_tiles = it.k_len > 0 ? (it.k_len + BN - 1) / BN : 0;
+  const int64_t HD = (int64_t)g.H * D;
+
+  if (tid == 0) {
+    mbar_init(bar(B_KFULL), 1);
+    mbar_init(bar(B_KFULL + 1), 1);
+    mbar_init(bar(B_KEMPTY), 1);
+    mbar_init(bar(B_KEMPTY + 1), 1);
+    mbar_init(bar(B_VFULL), 1);
+    mbar_init(bar(B_VFULL + 1), 1);
+    mbar_init(bar(B_VEMPTY), 1);
+    mbar_init(bar(B_VEMPTY + 1), 1);
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_SFULL + 1), 1);
+    mbar_init(bar(B_PFULL), 128);
+    mbar_init(bar(B_PFULL + 1), 128);
+    mbar_init(bar(B_PVDONE), 1);
+    mbar_init(bar(B_PVDONE + 1), 1);
+    mbar_init(bar(B_FIN), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (warp == 4 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&args.tk)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&args.tv)) : "memory");
+  }
+  if (warp < 4) {
+    // Q tile: thread i loads query row i (zeros past the item's queries)
+    // into the K-major 128-byte-swizzled layout.
+    const int r = tid;
+    const bool ok = r < it.nq;
+    const int tok = ok ? tc_query_token(it, g, r) : 0;
+    const int4* src = reinterpret_cast<const int4*>(static_cast<const bf16*>(p.q) + tok * HD + (int64_t)it.head * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      int4 v = ok ? __ldg(src + c) : make_int4(0, 0, 0, 0);
+      const uint32_t dst = sQ + (c >> 3) * L::Q_REG + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
+    fence_proxy_async();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && n_tiles > 0) {
+      const int ycoord = args.kv_head_coord ? it.head : 0;
+      int issued_k = 0, issued_v = 0;
+      volatile int zero_flag = 0;   // drains ignore the abort flag
+      for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % STAGES;
+        const uint32_t wpar = ((t / STAGES) - 1) & 1;
+        const int row = (int)(it.k_row0 + (int64_t)t * BN);
+        if (t >= STAGES && !mbar_wait_bounded(bar(B_KEMPTY + st), wpar, abort_flag, WAIT_LIMIT_NS)) break;
+        mbar_expect_tx(bar(B_KFULL + st), L::KV_BYTES);
+#pragma unroll
+        for (int rgn = 0; rgn < L::NREG; ++rgn)
+          tma_load_3d(sK + st * L::KV_BYTES + rgn * L::KV_REG, &args.tk, rgn * 64, ycoord, row, bar(B_KFULL + st));
+        issued_k = t + 1;
+        if (t >= STAGES && !mbar_wait_bounded(bar(B_VEMPTY + st), wpar, abort_flag, WAIT_LIMIT_NS)) break;
+        mbar_expect_tx(bar(B_VFULL + st), L::KV_BYTES);
+#pragma unroll
+        for (int rgn = 0; rgn < L::NREG; ++rgn)
+          tma_load_3d(sV + st * L::KV_BYTES + rgn * L::KV_REG, &args.tv, rgn * 64, ycoord, row, bar(B_VFULL + st));
+        issued_v = t + 1;
+      }
+      if (*abort_flag || issued_v < n_tiles) {
+        *abort_flag = 1;
+        // Let the copies still in flight land before the CTA's memory goes.
+        for (int t = max(0, issued_k - STAGES); t < issued_k; ++t)
+          (void)mbar_wait_bounded(bar(B_KFULL + t % STAGES), (t / STAGES) & 1, &zero_flag, DRAIN_LIMIT_NS);
+        for (int t = max(0, issued_v - STAGES); t < issued_v; ++t)
+          (void)mbar_wait_bounded(bar(B_VFULL + t % STAGES), (t / STAGES) & 1, &zero_flag, DRAIN_LIMIT_NS);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t ID_S = idesc_bf16(BM, BN, false);
+      constexpr uint32_t ID_PV = idesc_bf16(BM, D, true);
+      bool ok = true;
+      volatile int zero_flag = 0;
+      auto issue_s = [&](int t) -> bool {
+        const int st = t % STAGES, b = t & 1;
+        if (!mbar_wait_bounded(bar(B_KFULL + st), (t / STAGES) & 1, abort_flag, WAIT_LIMIT_NS)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks & 3) << 5;   // 16 columns = 32 B inside the 128-B row
+          const uint64_t a = sdesc(sQ + (ks >> 2) * L::Q_REG + off, 16, 1024);
+          const uint64_t bk = sdesc(sK + st * L::KV_BYTES + (ks >> 2) * L::KV_REG + off, 16, 1024);
+          mma_bf16_ss(tmem + b * BN, a, bk, ID_S, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B_KEMPTY + st));
+        mma_commit(bar(B_SFULL + b));
+        return true;
+      };
+      ok = issue_s(0);
+      if (ok && n_tiles > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int b = j & 1, st = j % STAGES;
+        if (!mbar_wait_bounded(bar(B_PFULL + b), (j >> 1) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
+        if (!mbar_wait_bounded(bar(B_VFULL + st), (j / STAGES) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          const uint64_t a = sdesc(sP + b * L::P_BYTES + (ks >> 2) * L::P_REG + ((ks & 3) << 5), 16, 1024);
+          const uint64_t bv = sdesc(sV + st * L::KV_BYTES + ks * 16 * 128, L::KV_REG, 1024);
+          mma_bf16_ss(tmem + L::COL_O, a, bv, ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(B_VEMPTY + st));
+        mma_commit(bar(B_PVDONE + b));
+        if (j + 2 < n_tiles) ok = issue_s(j + 2);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        // Every MMA issued so far must finish before TMEM is released.
+        mma_commit(bar(B_FIN));
+        (void)mbar_wait_bounded(bar(B_FIN), 0, &zero_flag, DRAIN_LIMIT_NS);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- softmax warpgroup
+    const int row = tid;                                 // query row == TMEM lane
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = g.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    auto wait_warp = [&](int slot, uint32_t parity) -> bool {
+      bool w = mbar_wait_bounded(bar(slot), parity, abort_flag, WAIT_LIMIT_NS);
+      return __all_sync(0xffffffffu, w);
+    };
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j & 1;
+      if (!wait_warp(B_SFULL + b, (j >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t s[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(t_lane + b * BN + c * 32, s + c * 32);
+      tmem_wait_ld();
+      const int valid = min(BN, it.k_len - j * BN);
+      if (valid < BN) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c >= valid) s[c] = __float_as_uint(-INFINITY);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+      const float m_new = fmaxf(m_run, mx * sl2);
+      if (j == 0) {
+        m_run = m_new;
+      } else if (__any_sync(0xffffffffu, m_new > m_run + RESCALE_LOG2)) {
+        // O holds P(0..j-1) V: wait for the last of those products, then
+        // scale this warp's rows of O to the new maximum.
+        if (!wait_warp(B_PVDONE + ((j - 1) & 1), ((j - 1) >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const float alpha = ex2(m_run - m_new);
+        l_run *= alpha;
+        m_run = m_new;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(t_lane + L::COL_O + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(t_lane + L::COL_O + c * 32, o);
+        }
+        tmem_wait_st();
+      }
+      // P buffer b was last read by P(j-2) V(j-2).
+      if (j >= 2 && !wait_warp(B_PVDONE + b, ((j - 2) >> 1) & 1)) { ok = false; break; }
+      const float neg_m = -m_run;
+      float rs = 0.f;
+      const uint32_t prow = sP + b * L::P_BYTES + row * 128;
+#pragma unroll
+      for (int c = 0; c < BN / 8; ++c) {
+        float e[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          e[u] = ex2(fmaf(__uint_as_float(s[c * 8 + u]), sl2, neg_m));
+          rs += e[u];
+        }
+        const uint32_t dst = prow + (c >> 3) * L::P_REG + (((c & 7) ^ (row & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pack_bf16(e[0], e[1])),
+                     "r"(pack_bf16(e[2], e[3])), "r"(pack_bf16(e[4], e[5])), "r"(pack_bf16(e[6], e[7]))
+                     : "memory");
+      }
+      l_run += rs;
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(bar(B_PFULL + b));
+    }
+    // ---------------------------------------------------------------- epilogue
+    if (ok && n_tiles > 0 && wait_warp(B_PVDONE + ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1)) {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const bool w = row < it.nq;
+      const int64_t tok = w ? tc_query_token(it, g, row) : 0;
+      const int64_t base = (int64_t)it.out_plane * p.o_plane_stride + tok * HD + (int64_t)it.head * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_lane + L::COL_O + c * 32, o);
+        tmem_wait_ld();
+        if (!w) continue;
+        if (p.out_fp32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + base + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                 __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(p.o) + base + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t* x = o + 8 * e;
+            dst[e] = make_uint4(pack_bf16(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                                pack_bf16(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                                pack_bf16(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                                pack_bf16(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+          }
+        }
+      }
+    } else if (n_tiles == 0 && row < it.nq) {
+      // No keys: the output is defined as zero.
+      const int64_t tok = tc_query_token(it, g, row);
+      const int64_t base = (int64_t)it.out_plane * p.o_plane_stride + tok * HD + (int64_t)it.head * D;
+      for (int c = 0; c < D; ++c) {
+        if (p.out_fp32) static_cast<float*>(p.o)[base + c] = 0.f;
+        else static_cast<bf16*>(p.o)[base + c] = __float2bfloat16_rn(0.f);
+      }
+    } else if (n_tiles > 0) {
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag && p.status) atomicExch(p.status, DEV_TIMEOUT);
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// K or V as a 3-D bf16 tensor [rows][heads][d]; box {64, 1, BN}, 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+  const cuuint32_t box[3] = {64, 1, BN};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t launch_d(const TcArgs& a, dim3 grid, cudaStream_t s) {
+  constexpr int smem = Layout<D>::ALLOC;
+  static_assert(smem <= 232448, "shared memory budget");
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr != cudaSuccess) return attr;
+  attn_tc_kernel<D><<<grid, NTHREADS, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_block_rows() { return BM; }
+
+cudaError_t launch_attention_tc(const AttnParams& p, const TcKV& kv, dim3 grid, cudaStream_t s) {
+  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
+  if (p.g.d != 64 && p.g.d != 128) return cudaErrorInvalidValue;
+  if (kv.rows <= 0 || kv.rows > 0x7fffffffll) return cudaErrorInvalidValue;
+  TcArgs a;
+  memset(&a, 0, sizeof a);
+  cudaError_t e = make_map(&a.tk, kv.k, p.g.d, kv.heads, kv.rows);
+  if (e != cudaSuccess) return e;
+  if ((e = make_map(&a.tv, kv.v, p.g.d, kv.heads, kv.rows)) != cudaSuccess) return e;
+  a.p = p;
+  a.kv_head_coord = kv.heads > 1 ? 1 : 0;
+  return p.g.d == 128 ? launch_d<128>(a, grid, s) : launch_d<64>(a, grid, s);
+}
+
+}  // namespace hc

@@ -105,6 +105,20 @@ enum : int { DEV_OK = 0, DEV_TIMEOUT = 7, DEV_BOUNDS = 6 };
 cudaError_t launch_attention(const AttnParams& p, int dtype, dim3 grid, cudaStream_t s);
 int attention_block_rows(int dtype, int d);   // queries per item tile
 
+// tcgen05/TMA attention (attn_tc.cu), bf16 only.  K and V are read as
+// [rows][heads][d] tensors; with heads == 1 the key rows of an item are
+// absolute rows of that buffer (the restructured cache), otherwise token
+// rows of a monolithic [tokens][H][d] window addressed with the item's head.
+struct TcKV {
+  const void* k;
+  const void* v;
+  int heads;
+  int64_t rows;
+};
+cudaError_t launch_attention_tc(const AttnParams& p, const TcKV& kv, dim3 grid, cudaStream_t s);
+int tc_block_rows();                          // queries per tcgen05 item (128)
+int proxy_block_rows();                       // queries per classification-proxy item
+
 // Classification post-processing (classify.cu).
 struct ClassifyPost {
   const float* planes;      // 4 planes fp32 [Nq][H][d]: full, sink, dummy, proxy
