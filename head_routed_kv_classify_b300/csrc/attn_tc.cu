@@ -11,20 +11,23 @@
 // contiguous run of key rows.  Roles (192 threads):
 //   warps 0-3  softmax: thread i owns query row i, i.e. TMEM lane i.  It
 //              reads its row of S = Q K^T from TMEM, keeps the running max
-//              and sum, writes P (bf16) to shared memory and, when the max
-//              has grown by more than 2^8, rescales its row of O in TMEM;
-//              at the end it normalises O and stores it.
-//   warp 4     TMA producer: K and V tiles of 128 keys into a 2-stage ring.
-//   warp 5     MMA issuer: S(j) = Q K(j)^T into one of two S buffers in
-//              TMEM, O += P(j) V(j) into the O accumulator in TMEM.
+//              and sum, writes P (bf16, two per 32-bit column) back to TMEM
+//              and, when the max has grown by more than 2^8, rescales its
+//              row of O in TMEM; at the end it normalises O and stores it.
+//   warp 4     TMA producer: K and V tiles of 128 keys into a 3-stage ring.
+//   warp 5     MMA issuer: S(j) = Q K(j)^T (both operands in shared memory)
+//              into one of two S buffers in TMEM; O += P(j) V(j) with P read
+//              from TMEM and V from shared memory.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,256+d), P0 [384,448),
+// P1 [448,512).
 // Hand-offs are mbarriers; every wait is bounded in wall-clock time and on
 // expiry the CTA records HC_ERR_TIMEOUT in the status word, drains its own
 // copies and MMAs (again bounded), frees TMEM and returns.
 //
 // Shared-memory operand layouts are the canonical 128-byte-swizzle ones:
-// Q, K and P are K-major (rows of 64 bf16 = 128 B, 8-row atoms of 1 KB,
-// one region per 64 columns); V is the MN-major B operand of P V (rows are
-// keys, 128 B per 64 channels of d).
+// Q and K are K-major (rows of 64 bf16 = 128 B, 8-row atoms of 1 KB, one
+// region per 64 columns); V is the MN-major B operand of P V (rows are keys,
+// 128 B per 64 channels of d).
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -40,7 +43,7 @@ typedef __nv_bfloat16 bf16;
 
 constexpr int BM = 128;            // queries per item (one MMA M)
 constexpr int BN = 128;            // keys per tile
-constexpr int STAGES = 2;          // K/V ring depth
+constexpr int STAGES = 3;          // K/V ring depth
 constexpr int NTHREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.f;  // rescale O when the row max grows by > 2^8
@@ -53,21 +56,19 @@ struct Layout {
   static constexpr int Q_REG = BM * 128;
   static constexpr int KV_REG = BN * 128;
   static constexpr int KV_BYTES = NREG * KV_REG;    // one K (or V) tile
-  static constexpr int P_REG = BM * 128;
-  static constexpr int P_BYTES = (BN / 64) * P_REG;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NREG * Q_REG;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   static constexpr int BYTES = OFF_BAR + 256;
   static constexpr int ALLOC = BYTES + 1024;        // room to align the base to 1 KB
   static constexpr uint32_t COL_O = 2 * BN;         // TMEM: S0 [0,BN), S1 [BN,2BN), O [2BN, 2BN+D)
+  static constexpr uint32_t COL_P = 384;            // P0 [384,448), P1 [448,512): BN bf16 per lane
 };
 
 // Barrier slots (8 bytes each) after OFF_BAR.
-enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_SFULL = 8, B_PFULL = 10,
-       B_PVDONE = 12, B_FIN = 14, B_COUNT = 15 };
+enum { B_KFULL = 0, B_KEMPTY = 3, B_VFULL = 6, B_VEMPTY = 9, B_SFULL = 12, B_PFULL = 14,
+       B_PVDONE = 16, B_FIN = 18, B_COUNT = 19 };
 
 struct TcArgs {
   CUtensorMap tk;        // K as [rows][heads][D] (3-D map, box {64, 1, BN})
@@ -107,9 +108,8 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 
 // Wait until phase `parity` of `bar` has completed, for at most `limit` ns
 // or until another role has raised the CTA's abort flag.
-__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                               unsigned long long limit) {
-  if (mbar_try(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            unsigned long long limit) {
   const unsigned long long t0 = now_ns();
   for (;;) {
 #pragma unroll 1
@@ -118,6 +118,12 @@ __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, vo
     if (*abort_flag) return false;
     if (now_ns() - t0 > limit) return false;
   }
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  unsigned long long limit) {
+  if (mbar_try(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, limit);
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -158,6 +164,14 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a, uint64_
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
       ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// As above with A (M x 16, K-major) read from TMEM at column a_tmem.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -262,7 +276,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
-  const uint32_t sQ = s_base + L::OFF_Q, sK = s_base + L::OFF_K, sV = s_base + L::OFF_V, sP = s_base + L::OFF_P;
+  const uint32_t sQ = s_base + L::OFF_Q, sK = s_base + L::OFF_K, sV = s_base + L::OFF_V;
   const uint32_t bars = s_base + L::OFF_BAR;
   auto bar = [&](int slot) { return bars + 8u * slot; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 8 * B_COUNT);
@@ -284,14 +298,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
   const int64_t HD = (int64_t)g.H * D;
 
   if (tid == 0) {
-    mbar_init(bar(B_KFULL), 1);
-    mbar_init(bar(B_KFULL + 1), 1);
-    mbar_init(bar(B_KEMPTY), 1);
-    mbar_init(bar(B_KEMPTY + 1), 1);
-    mbar_init(bar(B_VFULL), 1);
-    mbar_init(bar(B_VFULL + 1), 1);
-    mbar_init(bar(B_VEMPTY), 1);
-    mbar_init(bar(B_VEMPTY + 1), 1);
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(bar(B_KFULL + st), 1);
+      mbar_init(bar(B_KEMPTY + st), 1);
+      mbar_init(bar(B_VFULL + st), 1);
+      mbar_init(bar(B_VEMPTY + st), 1);
+    }
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_SFULL + 1), 1);
     mbar_init(bar(B_PFULL), 128);
@@ -397,9 +409,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t a = sdesc(sP + b * L::P_BYTES + (ks >> 2) * L::P_REG + ((ks & 3) << 5), 16, 1024);
+          // 16 keys of P = 8 packed columns of TMEM; 16 rows of V = 2 KB.
           const uint64_t bv = sdesc(sV + st * L::KV_BYTES + ks * 16 * 128, L::KV_REG, 1024);
-          mma_bf16_ss(tmem + L::COL_O, a, bv, ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + L::COL_O, tmem + L::COL_P + b * (BN / 2) + ks * 8, bv, ID_PV,
+                      (j > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(bar(B_VEMPTY + st));
         mma_commit(bar(B_PVDONE + b));
@@ -438,10 +451,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         for (int c = 0; c < BN; ++c)
           if (c >= valid) s[c] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      // Row max with 16 independent partial maxima (no serial chain).
+      float pm[16];
 #pragma unroll
-      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
-      const float m_new = fmaxf(m_run, mx * sl2);
+      for (int u = 0; u < 16; ++u) pm[u] = __uint_as_float(s[u]);
+#pragma unroll
+      for (int c = 16; c < BN; ++c) pm[c & 15] = fmaxf(pm[c & 15], __uint_as_float(s[c]));
+#pragma unroll
+      for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int u = 0; u < w; ++u) pm[u] = fmaxf(pm[u], pm[u + w]);
+      const float m_new = fmaxf(m_run, pm[0] * sl2);
       if (j == 0) {
         m_run = m_new;
       } else if (__any_sync(0xffffffffu, m_new > m_run + RESCALE_LOG2)) {
@@ -466,23 +486,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       // P buffer b was last read by P(j-2) V(j-2).
       if (j >= 2 && !wait_warp(B_PVDONE + b, ((j - 2) >> 1) & 1)) { ok = false; break; }
       const float neg_m = -m_run;
-      float rs = 0.f;
-      const uint32_t prow = sP + b * L::P_BYTES + row * 128;
+      float ps[8];   // 8 independent partial sums
 #pragma unroll
-      for (int c = 0; c < BN / 8; ++c) {
-        float e[8];
+      for (int u = 0; u < 8; ++u) ps[u] = 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          e[u] = ex2(fmaf(__uint_as_float(s[c * 8 + u]), sl2, neg_m));
-          rs += e[u];
+      for (int h = 0; h < BN / 64; ++h) {
+        uint32_t pk[32];   // 64 probabilities, two bf16 per column
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float e0 = ex2(fmaf(__uint_as_float(s[h * 64 + 2 * c]), sl2, neg_m));
+          const float e1 = ex2(fmaf(__uint_as_float(s[h * 64 + 2 * c + 1]), sl2, neg_m));
+          ps[(2 * c) & 7] += e0;
+          ps[(2 * c + 1) & 7] += e1;
+          pk[c] = pack_bf16(e0, e1);
         }
-        const uint32_t dst = prow + (c >> 3) * L::P_REG + (((c & 7) ^ (row & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pack_bf16(e[0], e[1])),
-                     "r"(pack_bf16(e[2], e[3])), "r"(pack_bf16(e[4], e[5])), "r"(pack_bf16(e[6], e[7]))
-                     : "memory");
+        tmem_st32(t_lane + L::COL_P + b * (BN / 2) + h * 32, pk);
       }
-      l_run += rs;
-      fence_proxy_async();
+      l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + b));
     }
