@@ -7,19 +7,27 @@
 //  only over its pathway), "What carries the argument" (the classification
 //  outputs), major comment 2 and Figure 3 caption (10x10 cells).]
 //
-// One CTA computes one work item: up to 128 queries of one head against one
-// contiguous run of key rows.  Roles (192 threads):
-//   warps 0-3  softmax: thread i owns query row i, i.e. TMEM lane i.  It
-//              reads its row of S = Q K^T from TMEM, keeps the running max
-//              and sum, writes P (bf16, two per 32-bit column) back to TMEM
-//              and, when the max has grown by more than 2^8, rescales its
-//              row of O in TMEM; at the end it normalises O and stores it.
-//   warp 4     TMA producer: K and V tiles of 128 keys into a 3-stage ring.
-//   warp 5     MMA issuer: S(j) = Q K(j)^T (both operands in shared memory)
-//              into one of two S buffers in TMEM; O += P(j) V(j) with P read
-//              from TMEM and V from shared memory.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,256+d), P0 [384,448),
-// P1 [448,512).
+// One CTA computes one work item: up to 256 queries of one head (two query
+// tiles of 128) against one contiguous run of key rows, streamed in tiles of
+// 128 keys.  Roles (320 threads):
+//   warps 0-3, 4-7  softmax groups, one per query tile: thread r of group i
+//              owns row r of tile i, i.e. TMEM lane r.  It reads its row of
+//              S_i = Q_i K^T from TMEM (a max pass, then an exponent pass),
+//              keeps the running max and sum, writes P_i (bf16, two per
+//              32-bit column) back over the first half of S_i and, when the
+//              max has grown by more than 2^8, rescales its row of O_i; at
+//              the end it normalises O_i and stores it.
+//   warp 8     TMA producer: K and V tiles into a 2-stage ring.
+//   warp 9     MMA issuer, in the order P_0 V, S_0, P_1 V, S_1 per key tile,
+//              so the tensor core always has the other tile's products
+//              queued while a softmax group works.  S uses Q and K from
+//              shared memory; P V reads P from TMEM and V from shared memory.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it.
+// P_i(j) overwrites S_i(j) once it has been read; S_i(j+1) is written there
+// only by an MMA issued after P_i(j) V(j), and MMAs issued by one thread
+// execute in order.  The commit that signals S_i(j) also covers
+// P_i(j-1) V(j-1), so a softmax group may rescale O_i as soon as it sees
+// S_i(j).
 // Hand-offs are mbarriers; every wait is bounded in wall-clock time and on
 // expiry the CTA records HC_ERR_TIMEOUT in the status word, drains its own
 // copies and MMAs (again bounded), frees TMEM and returns.
@@ -41,10 +49,12 @@ namespace {
 
 typedef __nv_bfloat16 bf16;
 
-constexpr int BM = 128;            // queries per item (one MMA M)
+constexpr int BM = 128;            // queries per tile (one MMA M)
+constexpr int QT = 2;              // query tiles per CTA
 constexpr int BN = 128;            // keys per tile
-constexpr int STAGES = 3;          // K/V ring depth
-constexpr int NTHREADS = 192;
+constexpr int STAGES = 2;          // K/V ring depth
+constexpr int NTHREADS = 320;
+constexpr int W_PRODUCER = 8, W_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.f;  // rescale O when the row max grows by > 2^8
 constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;   // 1 s
@@ -54,21 +64,22 @@ template <int D>
 struct Layout {
   static constexpr int NREG = D / 64;               // 64-column regions along d
   static constexpr int Q_REG = BM * 128;
+  static constexpr int Q_BYTES = NREG * Q_REG;       // one query tile
   static constexpr int KV_REG = BN * 128;
   static constexpr int KV_BYTES = NREG * KV_REG;    // one K (or V) tile
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + NREG * Q_REG;
+  static constexpr int OFF_K = OFF_Q + QT * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   static constexpr int BYTES = OFF_BAR + 256;
   static constexpr int ALLOC = BYTES + 1024;        // room to align the base to 1 KB
-  static constexpr uint32_t COL_O = 2 * BN;         // TMEM: S0 [0,BN), S1 [BN,2BN), O [2BN, 2BN+D)
-  static constexpr uint32_t COL_P = 384;            // P0 [384,448), P1 [448,512): BN bf16 per lane
+  static constexpr uint32_t COL_O = QT * BN;        // O_i at COL_O + i * D
+  static_assert(COL_O + QT * D <= TMEM_COLS, "TMEM budget");
 };
 
 // Barrier slots (8 bytes each) after OFF_BAR.
-enum { B_KFULL = 0, B_KEMPTY = 3, B_VFULL = 6, B_VEMPTY = 9, B_SFULL = 12, B_PFULL = 14,
-       B_PVDONE = 16, B_FIN = 18, B_COUNT = 19 };
+enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_SFULL = 8, B_PFULL = 10,
+       B_ODONE = 12, B_FIN = 14, B_COUNT = 15 };
 
 struct TcArgs {
   CUtensorMap tk;        // K as [rows][heads][D] (3-D map, box {64, 1, BN})
@@ -212,6 +223,26 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// (d0, d1) = (a0, a1) * b + c as one packed two-lane fp32 FMA.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %4};\n mov.b64 rc, {%5, %5};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (s0, s1) += (a0, a1) as one packed two-lane fp32 add.
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+  asm("{\n .reg .b64 rs, ra;\n mov.b64 rs, {%0, %1};\n mov.b64 ra, {%2, %3};\n add.rn.f32x2 rs, rs, ra;\n"
+      " mov.b64 {%0, %1}, rs;\n}\n"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -249,8 +280,8 @@ __device__ __forceinline__ TcItem tc_decode(const AttnParams& p) {
   } else {  // ITEMS_DENSE
     it.head = blockIdx.y;
     it.kind = ITEM_RANGE;
-    it.q0 = blockIdx.x * BM;
-    it.nq = min(BM, p.nq_total - it.q0);
+    it.q0 = blockIdx.x * (QT * BM);
+    it.nq = min(QT * BM, p.nq_total - it.q0);
     it.out_plane = blockIdx.z;
     it.k_row0 = p.plane_k0[blockIdx.z];
     it.k_len = p.plane_klen[blockIdx.z];
@@ -281,7 +312,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
   auto bar = [&](int slot) { return bars + 8u * slot; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 * B_COUNT + 4);
-
   volatile int* skip_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 * B_COUNT + 8);
 
   const AttnParams& p = args.p;
@@ -295,6 +325,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
   const TcItem it = tc_decode(p);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = it.k_len > 0 ? (it.k_len + BN - 1) / BN : 0;
+  const bool two = it.nq > BM;   // second query tile in use
   const int64_t HD = (int64_t)g.H * D;
 
   if (tid == 0) {
@@ -304,37 +335,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       mbar_init(bar(B_VFULL + st), 1);
       mbar_init(bar(B_VEMPTY + st), 1);
     }
-    mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_SFULL + 1), 1);
-    mbar_init(bar(B_PFULL), 128);
-    mbar_init(bar(B_PFULL + 1), 128);
-    mbar_init(bar(B_PVDONE), 1);
-    mbar_init(bar(B_PVDONE + 1), 1);
+    for (int i = 0; i < QT; ++i) {
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_PFULL + i), 128);
+      mbar_init(bar(B_ODONE + i), 1);
+    }
     mbar_init(bar(B_FIN), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 5) {
+  if (warp == W_MMA) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(TMEM_COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == W_PRODUCER && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&args.tk)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&args.tv)) : "memory");
   }
-  if (warp < 4) {
-    // Q tile: thread i loads query row i (zeros past the item's queries)
-    // into the K-major 128-byte-swizzled layout.
-    const int r = tid;
-    const bool ok = r < it.nq;
-    const int tok = ok ? tc_query_token(it, g, r) : 0;
+  if (warp < 4 * QT) {
+    // Query tiles: thread r of group i loads row i*128 + r of the item
+    // (zeros past its queries) into the K-major 128-byte-swizzled layout.
+    const int grp = warp >> 2, r = tid & 127, qrow = grp * BM + r;
+    const bool ok = qrow < it.nq;
+    const int tok = ok ? tc_query_token(it, g, qrow) : 0;
     const int4* src = reinterpret_cast<const int4*>(static_cast<const bf16*>(p.q) + tok * HD + (int64_t)it.head * D);
+    const uint32_t q_tile = sQ + grp * L::Q_BYTES;
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       int4 v = ok ? __ldg(src + c) : make_int4(0, 0, 0, 0);
-      const uint32_t dst = sQ + (c >> 3) * L::Q_REG + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+      const uint32_t dst = q_tile + (c >> 3) * L::Q_REG + r * 128 + (((c & 7) ^ (r & 7)) << 4);
       asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                    : "memory");
     }
@@ -345,12 +376,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == W_PRODUCER) {
     // ---------------------------------------------------------------- producer
     if (lane == 0 && n_tiles > 0) {
       const int ycoord = args.kv_head_coord ? it.head : 0;
       int issued_k = 0, issued_v = 0;
-      volatile int zero_flag = 0;   // drains ignore the abort flag
       for (int t = 0; t < n_tiles; ++t) {
         const int st = t % STAGES;
         const uint32_t wpar = ((t / STAGES) - 1) & 1;
@@ -371,6 +401,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       if (*abort_flag || issued_v < n_tiles) {
         *abort_flag = 1;
         // Let the copies still in flight land before the CTA's memory goes.
+        volatile int zero_flag = 0;   // drains ignore the abort flag
         for (int t = max(0, issued_k - STAGES); t < issued_k; ++t)
           (void)mbar_wait_bounded(bar(B_KFULL + t % STAGES), (t / STAGES) & 1, &zero_flag, DRAIN_LIMIT_NS);
         for (int t = max(0, issued_v - STAGES); t < issued_v; ++t)
@@ -378,146 +409,196 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == W_MMA) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t ID_S = idesc_bf16(BM, BN, false);
       constexpr uint32_t ID_PV = idesc_bf16(BM, D, true);
-      bool ok = true;
-      volatile int zero_flag = 0;
-      auto issue_s = [&](int t) -> bool {
-        const int st = t % STAGES, b = t & 1;
-        if (!mbar_wait_bounded(bar(B_KFULL + st), (t / STAGES) & 1, abort_flag, WAIT_LIMIT_NS)) return false;
-        tc_fence_after();
+      // Descriptors of query tile 0 and of the first K and V stage; the
+      // start-address field is advanced by (byte offset >> 4), which cannot
+      // carry out of its 14 bits (shared addresses stay below 256 KB).
+      const uint64_t dq0 = sdesc(sQ, 16, 1024);
+      const uint64_t dk0 = sdesc(sK, 16, 1024);
+      const uint64_t dv0 = sdesc(sV, L::KV_REG, 1024);
+      auto wait1 = [&](int slot, uint32_t parity) {
+        return mbar_wait_bounded(bar(slot), parity, abort_flag, WAIT_LIMIT_NS);
+      };
+      // S_i(t) = Q_i K(t)^T into S_i's TMEM columns.
+      auto mma_s = [&](int i, int t) {
+        const uint64_t dk = dk0 + ((uint32_t)((t % STAGES) * L::KV_BYTES) >> 4);
+        const uint64_t dq = dq0 + ((uint32_t)(i * L::Q_BYTES) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks & 3) << 5;   // 16 columns = 32 B inside the 128-B row
-          const uint64_t a = sdesc(sQ + (ks >> 2) * L::Q_REG + off, 16, 1024);
-          const uint64_t bk = sdesc(sK + st * L::KV_BYTES + (ks >> 2) * L::KV_REG + off, 16, 1024);
-          mma_bf16_ss(tmem + b * BN, a, bk, ID_S, ks > 0 ? 1u : 0u);
+          // 16 columns of d = 32 B inside the 128-B row of region ks / 4.
+          const uint32_t koff = (ks >> 2) * L::KV_REG + ((ks & 3) << 5);
+          const uint32_t qoff = (ks >> 2) * L::Q_REG + ((ks & 3) << 5);
+          mma_bf16_ss(tmem + i * BN, dq + (qoff >> 4), dk + (koff >> 4), ID_S, ks > 0 ? 1u : 0u);
         }
-        mma_commit(bar(B_KEMPTY + st));
-        mma_commit(bar(B_SFULL + b));
-        return true;
+        mma_commit(bar(B_SFULL + i));
       };
-      ok = issue_s(0);
-      if (ok && n_tiles > 1) ok = issue_s(1);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int b = j & 1, st = j % STAGES;
-        if (!mbar_wait_bounded(bar(B_PFULL + b), (j >> 1) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
-        if (!mbar_wait_bounded(bar(B_VFULL + st), (j / STAGES) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
-        tc_fence_after();
+      // O_i += P_i(j) V(j), P_i from the first half of S_i's columns.
+      auto mma_pv = [&](int i, int j) {
+        const uint64_t dv = dv0 + ((uint32_t)((j % STAGES) * L::KV_BYTES) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          // 16 keys of P = 8 packed columns of TMEM; 16 rows of V = 2 KB.
-          const uint64_t bv = sdesc(sV + st * L::KV_BYTES + ks * 16 * 128, L::KV_REG, 1024);
-          mma_bf16_ts(tmem + L::COL_O, tmem + L::COL_P + b * (BN / 2) + ks * 8, bv, ID_PV,
+        for (int ks = 0; ks < BN / 16; ++ks)
+          mma_bf16_ts(tmem + L::COL_O + i * D, tmem + i * BN + ks * 8, dv + ((ks * 16 * 128) >> 4), ID_PV,
                       (j > 0 || ks > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(B_VEMPTY + st));
-        mma_commit(bar(B_PVDONE + b));
-        if (j + 2 < n_tiles) ok = issue_s(j + 2);
+      };
+      bool ok = wait1(B_KFULL, 0);
+      if (ok) {
+        tc_fence_after();
+        mma_s(0, 0);
+        if (two) mma_s(1, 0);
+        mma_commit(bar(B_KEMPTY));
       }
-      if (!ok) {
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j % STAGES;
+        const int nst = (j + 1) % STAGES;
+        const bool more = j + 1 < n_tiles;
+        if (!(ok = wait1(B_VFULL + st, (j / STAGES) & 1))) break;
+        if (!(ok = wait1(B_PFULL + 0, j & 1))) break;
+        tc_fence_after();
+        mma_pv(0, j);
+        if (!two) mma_commit(bar(B_VEMPTY + st));
+        if (more) {
+          if (!(ok = wait1(B_KFULL + nst, ((j + 1) / STAGES) & 1))) break;
+          tc_fence_after();
+          mma_s(0, j + 1);
+          if (!two) mma_commit(bar(B_KEMPTY + nst));
+        }
+        if (two) {
+          if (!(ok = wait1(B_PFULL + 1, j & 1))) break;
+          tc_fence_after();
+          mma_pv(1, j);
+          mma_commit(bar(B_VEMPTY + st));
+          if (more) {
+            mma_s(1, j + 1);
+            mma_commit(bar(B_KEMPTY + nst));
+          }
+        }
+      }
+      if (ok) {
+        mma_commit(bar(B_ODONE + 0));
+        if (two) mma_commit(bar(B_ODONE + 1));
+      } else {
         *abort_flag = 1;
         // Every MMA issued so far must finish before TMEM is released.
+        volatile int zero_flag = 0;
         mma_commit(bar(B_FIN));
         (void)mbar_wait_bounded(bar(B_FIN), 0, &zero_flag, DRAIN_LIMIT_NS);
       }
     }
     __syncwarp();
-  } else {
-    // ---------------------------------------------------------------- softmax warpgroup
-    const int row = tid;                                 // query row == TMEM lane
-    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+  } else if (warp < 4 * QT) {
+    // ---------------------------------------------------------------- softmax groups
+    const int grp = warp >> 2, r = tid & 127, qrow = grp * BM + r;
+    const bool active = grp == 0 || two;
+    const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t t_s = t_lane + grp * BN;            // S_i (and P_i over its first half)
+    const uint32_t t_o = t_lane + L::COL_O + grp * D;  // O_i
     const float sl2 = g.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     auto wait_warp = [&](int slot, uint32_t parity) -> bool {
-      bool w = mbar_wait_bounded(bar(slot), parity, abort_flag, WAIT_LIMIT_NS);
+      const bool w = mbar_wait_bounded(bar(slot), parity, abort_flag, WAIT_LIMIT_NS);
       return __all_sync(0xffffffffu, w);
     };
-    for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1;
-      if (!wait_warp(B_SFULL + b, (j >> 1) & 1)) { ok = false; break; }
+    for (int j = 0; active && j < n_tiles; ++j) {
+      if (!wait_warp(B_SFULL + grp, j & 1)) { ok = false; break; }
       tc_fence_after();
-      uint32_t s[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(t_lane + b * BN + c * 32, s + c * 32);
-      tmem_wait_ld();
       const int valid = min(BN, it.k_len - j * BN);
-      if (valid < BN) {
+      const bool full = valid == BN;   // only a key run's last tile is partial
+      // Pass 1: row max over the tile (8 independent partial maxima,
+      // three-input max).
+      float pm[8];
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c >= valid) s[c] = __float_as_uint(-INFINITY);
+      for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t x[32];
+        tmem_ld32(t_s + c * 32, x);
+        tmem_wait_ld();
+        if (!full) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e >= valid) x[e] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          pm[u] = max3f(pm[u], __uint_as_float(x[4 * u]), __uint_as_float(x[4 * u + 1]));
+          pm[u] = max3f(pm[u], __uint_as_float(x[4 * u + 2]), __uint_as_float(x[4 * u + 3]));
+        }
       }
-      // Row max with 16 independent partial maxima (no serial chain).
-      float pm[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) pm[u] = __uint_as_float(s[u]);
-#pragma unroll
-      for (int c = 16; c < BN; ++c) pm[c & 15] = fmaxf(pm[c & 15], __uint_as_float(s[c]));
-#pragma unroll
-      for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-        for (int u = 0; u < w; ++u) pm[u] = fmaxf(pm[u], pm[u + w]);
-      const float m_new = fmaxf(m_run, pm[0] * sl2);
+      pm[0] = max3f(pm[0], pm[1], pm[2]);
+      pm[3] = max3f(pm[3], pm[4], pm[5]);
+      pm[6] = fmaxf(pm[6], pm[7]);
+      const float m_new = fmaxf(m_run, max3f(pm[0], pm[3], pm[6]) * sl2);
       if (j == 0) {
         m_run = m_new;
       } else if (__any_sync(0xffffffffu, m_new > m_run + RESCALE_LOG2)) {
-        // O holds P(0..j-1) V: wait for the last of those products, then
-        // scale this warp's rows of O to the new maximum.
-        if (!wait_warp(B_PVDONE + ((j - 1) & 1), ((j - 1) >> 1) & 1)) { ok = false; break; }
-        tc_fence_after();
+        // O_i holds P_i(0..j-1) V, all of it complete (the commit that
+        // signalled S_i(j) covers it): scale this warp's rows to the new max.
         const float alpha = ex2(m_run - m_new);
         l_run *= alpha;
         m_run = m_new;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          tmem_ld32(t_lane + L::COL_O + c * 32, o);
+          tmem_ld32(t_o + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(t_lane + L::COL_O + c * 32, o);
+          tmem_st32(t_o + c * 32, o);
         }
         tmem_wait_st();
       }
-      // P buffer b was last read by P(j-2) V(j-2).
-      if (j >= 2 && !wait_warp(B_PVDONE + b, ((j - 2) >> 1) & 1)) { ok = false; break; }
+      // Pass 2: probabilities 2^(s*scale*log2e - m), 64 keys at a time,
+      // packed two per column into P_i.  Masked keys become -inf, whose
+      // exponent is 0.
       const float neg_m = -m_run;
-      float ps[8];   // 8 independent partial sums
+      float ps[8];   // 4 independent pairs of partial sums
 #pragma unroll
       for (int u = 0; u < 8; ++u) ps[u] = 0.f;
 #pragma unroll
       for (int h = 0; h < BN / 64; ++h) {
-        uint32_t pk[32];   // 64 probabilities, two bf16 per column
+        // Keys [64h, 64h+64) of S_i; their probabilities go to P_i columns
+        // [32h, 32h+32), which lie inside S_i columns already read.
+        uint32_t x[64];
+        tmem_ld32(t_s + h * 64, x);
+        tmem_ld32(t_s + h * 64 + 32, x + 32);
+        tmem_wait_ld();
+        if (!full) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
+        }
+        uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float e0 = ex2(fmaf(__uint_as_float(s[h * 64 + 2 * c]), sl2, neg_m));
-          const float e1 = ex2(fmaf(__uint_as_float(s[h * 64 + 2 * c + 1]), sl2, neg_m));
-          ps[(2 * c) & 7] += e0;
-          ps[(2 * c + 1) & 7] += e1;
+          float a0, a1;
+          fma2(a0, a1, __uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1]), sl2, neg_m);
+          const float e0 = ex2(a0), e1 = ex2(a1);
+          add2(ps[2 * (c & 3)], ps[2 * (c & 3) + 1], e0, e1);
           pk[c] = pack_bf16(e0, e1);
         }
-        tmem_st32(t_lane + L::COL_P + b * (BN / 2) + h * 32, pk);
+        tmem_st32(t_s + h * 32, pk);
       }
       l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL + b));
+      mbar_arrive(bar(B_PFULL + grp));
     }
     // ---------------------------------------------------------------- epilogue
-    if (ok && n_tiles > 0 && wait_warp(B_PVDONE + ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1)) {
+    if (active && ok && n_tiles > 0 && wait_warp(B_ODONE + grp, 0)) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const bool w = row < it.nq;
-      const int64_t tok = w ? tc_query_token(it, g, row) : 0;
+      const bool w = qrow < it.nq;
+      const int64_t tok = w ? tc_query_token(it, g, qrow) : 0;
       const int64_t base = (int64_t)it.out_plane * p.o_plane_stride + tok * HD + (int64_t)it.head * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(t_lane + L::COL_O + c * 32, o);
+        tmem_ld32(t_o + c * 32, o);
         tmem_wait_ld();
         if (!w) continue;
         if (p.out_fp32) {
@@ -538,15 +619,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
           }
         }
       }
-    } else if (n_tiles == 0 && row < it.nq) {
+    } else if (active && n_tiles == 0 && qrow < it.nq) {
       // No keys: the output is defined as zero.
-      const int64_t tok = tc_query_token(it, g, row);
+      const int64_t tok = tc_query_token(it, g, qrow);
       const int64_t base = (int64_t)it.out_plane * p.o_plane_stride + tok * HD + (int64_t)it.head * D;
       for (int c = 0; c < D; ++c) {
         if (p.out_fp32) static_cast<float*>(p.o)[base + c] = 0.f;
         else static_cast<bf16*>(p.o)[base + c] = __float2bfloat16_rn(0.f);
       }
-    } else if (n_tiles > 0) {
+    } else if (active && n_tiles > 0) {
       *abort_flag = 1;
     }
   }
@@ -554,7 +635,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && *abort_flag && p.status) atomicExch(p.status, DEV_TIMEOUT);
-  if (warp == 5) {
+  if (warp == W_MMA) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
   }
@@ -610,7 +691,7 @@ cudaError_t launch_d(const TcArgs& a, dim3 grid, cudaStream_t s) {
 
 }  // namespace
 
-int tc_block_rows() { return BM; }
+int tc_block_rows() { return QT * BM; }
 
 cudaError_t launch_attention_tc(const AttnParams& p, const TcKV& kv, dim3 grid, cudaStream_t s) {
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
