@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     }
     for (int i = 0; i < QT; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_PFULL + i), 128);
+      mbar_init(bar(B_PFULL + i), 4);   // one arrival per softmax warp
       mbar_init(bar(B_ODONE + i), 1);
     }
     mbar_init(bar(B_FIN), 1);
@@ -586,7 +586,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL + grp));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL + grp));
     }
     // ---------------------------------------------------------------- epilogue
     if (active && ok && n_tiles > 0 && wait_warp(B_ODONE + grp, 0)) {
