@@ -54,11 +54,13 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="720p", choices=["480p", "720p", "1080p"])
+    ap.add_argument("--workload", default="720p", choices=["480p", "720p", "1080p", "rollout"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-paths", action="store_true",
+                    help="skip the per-pathway timing (every head on one pathway)")
     return ap.parse_args()
 
 
@@ -105,6 +107,38 @@ def routed_bytes(shape, labels, esize=2):
         rows = nq if a in (synth.SINK, synth.DUMMY) else shape.n_k
         kv += 2 * rows * d * esize
     return kv + 2 * nq * shape.n_heads * d * esize
+
+
+def path_measurements(hc, shape, cfg, k, v, q, o, flush, stream, reps, peak_tf, peak_bw):
+    """Routed attention with every head on one pathway (the per-path rows of
+    the method): mean CUDA-event time over `reps` launches, L2 flushed before
+    each, with its algorithmic FLOP and byte rates against the measured peaks."""
+    import torch
+    out = {}
+    for arch, name in ((synth.SINK, "sink"), (synth.DUMMY, "dummy"), (synth.SPATIAL, "spatial"),
+                       (synth.GLOBAL, "global")):
+        labels = [arch] * shape.n_heads
+        cache = hc.hc_cache_create(cfg, labels, device=q.device)
+        cache.restructure(k, v, 0)
+        times = []
+        for i in range(reps + 3):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            cache.routed_attention(q, o)
+            b.record(stream)
+            if i >= 3:
+                times.append((a, b))
+        torch.cuda.synchronize()
+        ms = statistics.mean(x.elapsed_time(y) for x, y in times)
+        fl, by = routed_flops(shape, labels), routed_bytes(shape, labels)
+        out[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "gbs": by / (ms * 1e-3) / 1e9,
+                     "frac_tensor": fl / (ms * 1e-3) / 1e12 / peak_tf,
+                     "frac_hbm": by / (ms * 1e-3) / 1e9 / peak_bw,
+                     "flops": fl, "bytes": by}
+        cache.close()
+        del cache
+    return out
 
 
 class ClockSampler:
@@ -255,6 +289,146 @@ def run_reference(args, shape, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- 30-layer rollout
+
+def run_rollout(args, rank, world, local_rank):
+    """The 30-layer 720P rollout: every layer holds its own restructured cache
+    (per-(layer, head) archetypes drawn from the seed), then 7 further AR
+    blocks x 4 denoising steps of append + routed attention run over all 30
+    layers.  One timed step is one denoising step of the whole stack (30
+    appends + 30 routed launches).  Classification (once per layer) is timed
+    separately, as the pages report it, and the same steps are run through
+    the library's full attention over monolithic per-layer rings.
+
+    Inputs: one seeded window per run (its K/V fill every layer's cache) and a
+    pool of 4 seeded blocks that the (layer, block, step) triples cycle
+    through; fresh draws for all 840 triples would be 83 GB of host data."""
+    import torch
+    import head_routed_kv_classify_b300 as hc
+    from head_routed_kv_classify_b300 import build as hcb
+
+    if not os.path.exists(hc.LIB_PATH):
+        hcb.build()
+    hc.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    R = synth.ROLLOUT_720P
+    shape, L, NB, NS = R["shape"], R["layers"], R["blocks"], R["steps"]
+    mix = synth.rollout_mix(L, shape.n_heads, R["seed"] + 1000 * rank)
+
+    def to_dev(x):
+        return torch.from_numpy(x.raw.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+
+    win = synth.make_layer(shape, seed=R["seed"] + 1000 * rank)
+    k, v, q0 = to_dev(win.k), to_dev(win.v), to_dev(win.q)
+    cfg = hc.config_for(shape)
+    pool = [synth.make_block(shape, seed=R["seed"] + 50 + i + 1000 * rank, mix=mix[0]) for i in range(4)]
+    qb = [to_dev(b[0]) for b in pool]
+    kb = [to_dev(b[1]) for b in pool]
+    vb = [to_dev(b[2]) for b in pool]
+    o = torch.empty_like(q0)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    # One-time phase: classification of every layer, then restructure.
+    scratch = torch.empty(hc.hc_classify_scratch_bytes(cfg), dtype=torch.uint8, device=dev)
+    labels_dev = torch.empty(shape.n_heads, dtype=torch.int8, device=dev)
+    hc.hc_classify(cfg, q0, k, v, labels_dev=labels_dev, scratch=scratch, copy_labels=False)
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for layer in range(L):
+        hc.hc_classify(cfg, q0, k, v, labels_dev=labels_dev, scratch=scratch, copy_labels=False)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    classify_ms = e0.elapsed_time(e1)
+    caches = []
+    for layer in range(L):
+        c = hc.hc_cache_create(cfg, mix[layer], device=dev)
+        c.restructure(k, v, 0)
+        caches.append(c)
+    first = shape.blocks_per_window
+    cache_bytes = sum(c.info()["bytes"] for c in caches)
+    mono_bytes = sum(c.info()["monolithic_bytes"] for c in caches)
+
+    def step(s, routed=True):
+        blk, st = divmod(s, NS)
+        for layer in range(L):
+            i = (layer + blk + st) % 4
+            caches[layer].append(first + blk, kb[i], vb[i])
+            caches[layer].routed_attention(qb[i], o)
+
+    for s in range(min(args.warmup, NS)):
+        step(s)
+    torch.cuda.synchronize()
+    hc.hc_get_last_error()
+    clock = ClockSampler(local_rank) if rank == 0 else None
+    if clock:
+        clock.start()
+    n_steps = NB * NS
+    evs = [(ev(), ev()) for _ in range(n_steps)]
+    torch.cuda.synchronize()
+    for s in range(n_steps):
+        evs[s][0].record(stream)
+        step(s)
+        evs[s][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = clock.stop() if clock else None
+    hc.hc_get_last_error()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(step_ms)
+
+    # The same steps through full attention over per-layer monolithic rings.
+    rings = [(k.clone(), v.clone()) for _ in range(L)]
+    full_steps = min(n_steps, 8)
+    fe = [(ev(), ev()) for _ in range(full_steps)]
+    for s in range(full_steps):
+        blk, st = divmod(s, NS)
+        slot = (first + blk) % shape.blocks_per_window
+        rows = slice(slot * shape.n_q, (slot + 1) * shape.n_q)
+        fe[s][0].record(stream)
+        for layer in range(L):
+            i = (layer + blk + st) % 4
+            kr, vr = rings[layer]
+            kr[rows].copy_(kb[i], non_blocking=True)
+            vr[rows].copy_(vb[i], non_blocking=True)
+            hc.hc_full_attention(cfg, qb[i], kr, vr, o=o)
+        fe[s][1].record(stream)
+    torch.cuda.synchronize()
+    full_step_ms = statistics.mean(a.elapsed_time(b) for a, b in fe)
+    if rank != 0:
+        return
+    peak_tf, peak_bw, peak_kind = measured_peaks()
+    flops = sum(routed_flops(shape, list(mix[layer])) for layer in range(L))
+    achieved = flops / (statistics.mean(step_ms) * 1e-3) / 1e12
+    value = world * L * shape.n_q * n_steps / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n_steps,
+        "warmup": min(args.warmup, NS), "ms_per_step": total_ms / n_steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) window and a pool of 4 seeded blocks; 720P shapes)",
+        "config": {"workload": "720p rollout", "layers": L, "n_heads": shape.n_heads,
+                   "head_dim": shape.head_dim, "frame": f"{shape.frame_h}x{shape.frame_w}",
+                   "blocks": NB, "denoising_steps": NS, "window_frames": shape.window_frames,
+                   "step": "30 x (hc_cache_append + hc_routed_attention)",
+                   "l2": f"inputs larger than L2 (30 layers' caches, {cache_bytes / 1e9:.1f} GB)",
+                   "head_mix": "uniform over the 4 archetypes per (layer, head), seed 4"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": None,
+                     "kernel": "one denoising step (30 appends + 30 routed launches)",
+                     "algorithmic_flops_per_step": flops,
+                     "peak_source": f"{peak_kind} bf16 dense (burst)"},
+        "gpu_launches": 2 * L * n_steps, "clocks": clocks,
+        "full_attention_step_ms": full_step_ms,
+        "step_speedup_vs_full": full_step_ms / (total_ms / n_steps),
+        "classify_ms_all_layers": classify_ms,
+        "classification_overhead_pct": 100.0 * classify_ms / (classify_ms + total_ms),
+        "cache_bytes": cache_bytes, "monolithic_cache_bytes": mono_bytes,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------------------- our arm
 
 def run_ours(args, shape, rank, world, local_rank):
@@ -382,6 +556,11 @@ def run_ours(args, shape, rank, world, local_rank):
     full_ms = [a.elapsed_time(b) for a, b in full_ms]
     mono_ms = [a.elapsed_time(b) for a, b in mono_ms]
 
+    peak_tf, peak_bw, peak_kind = measured_peaks()
+    paths = None
+    if not args.no_paths:
+        paths = path_measurements(hc, shape, cfg, k, v, q, o, flush, stream, 10, peak_tf, peak_bw)
+
     # End to end through the same public calls from pinned host buffers.
     e2e = None
     if args.e2e_steps > 0:
@@ -414,7 +593,6 @@ def run_ours(args, shape, rank, world, local_rank):
 
     if rank != 0:
         return
-    peak_tf, peak_bw, peak_kind = measured_peaks()
     flops = routed_flops(shape, labels)
     mean_routed = statistics.mean(routed_ms)
     achieved = flops / (mean_routed * 1e-3) / 1e12
@@ -443,6 +621,7 @@ def run_ours(args, shape, rank, world, local_rank):
         "step_speedup_vs_full": (statistics.mean(full_ms) + statistics.mean(mono_ms)) /
                                 (total_ms / args.steps),
         "classify_ms": classify_ms, "restructure_ms": restructure_ms,
+        "paths": paths,
         "wall_s_timed": wall,
     }
     if not args.no_cpu_baseline:
@@ -455,7 +634,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    shape = synth.SHAPES[args.workload]
+    shape = synth.SHAPES[args.workload if args.workload != "rollout" else "720p"]
     if args.impl == "reference":
         run_reference(args, shape, rank, world)
         return
@@ -464,7 +643,10 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    run_ours(args, shape, rank, world, local_rank)
+    if args.workload == "rollout":
+        run_rollout(args, rank, world, local_rank)
+    else:
+        run_ours(args, shape, rank, world, local_rank)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
