@@ -342,12 +342,19 @@ hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const 
     HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3((g.blk + BM - 1) / BM, g.H, 3), st),
             "classification attention");
   }
-  const int PBM = hc::proxy_block_rows();
   p.item_mode = hc::ITEMS_PROXY;
   p.proxy_frames = n_key_frames;
-  p.tiles_per_frame = (g.F + PBM - 1) / PBM;
-  HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3(g.fpb * p.tiles_per_frame, g.H, 1), st),
-          "classification proxy attention");
+  if (cfg->dtype == HC_BF16) {
+    p.tiles_per_frame = (g.F + BM - 1) / BM;
+    const hc::TcKV kv{k, v, g.H, nk};
+    HC_CUDA(hc::launch_attention_tc(p, kv, dim3(g.fpb * p.tiles_per_frame, g.H, 1), st),
+            "classification proxy attention");
+  } else {
+    const int PBM = hc::proxy_block_rows();
+    p.tiles_per_frame = (g.F + PBM - 1) / PBM;
+    HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3(g.fpb * p.tiles_per_frame, g.H, 1), st),
+            "classification proxy attention");
+  }
 
   hc::ClassifyPost c;
   std::memset(&c, 0, sizeof c);

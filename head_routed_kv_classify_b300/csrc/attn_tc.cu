@@ -28,6 +28,9 @@
 // execute in order.  The commit that signals S_i(j) also covers
 // P_i(j-1) V(j-1), so a softmax group may rescale O_i as soon as it sees
 // S_i(j).
+// The classification proxy (ITEMS_PROXY) runs the same pipeline on the band
+// of frame rows around a run of query tokens in every window frame, with a
+// per-row (2r+1) x (2r+1) neighbourhood mask applied to S before the softmax.
 // Hand-offs are mbarriers; every wait is bounded in wall-clock time and on
 // expiry the CTA records HC_ERR_TIMEOUT in the status word, drains its own
 // copies and MMAs (again bounded), frees TMEM and returns.
@@ -255,13 +258,31 @@ struct TcItem {
   int64_t k_row0;
   int k_len;
   int h0, w0, hz, wz;   // ITEM_CELL: the cell
+  int rlo, rlen, tpf;   // ITEM_PROXY: first band row, keys per frame band, key tiles per frame
 };
 
 __device__ __forceinline__ TcItem tc_decode(const AttnParams& p) {
   const Geom& g = p.g;
   TcItem it;
   it.h0 = it.w0 = it.hz = it.wz = 0;
-  if (p.item_mode == ITEMS_LIST) {
+  it.rlo = it.rlen = it.tpf = 0;
+  if (p.item_mode == ITEMS_PROXY) {
+    // Up to 256 consecutive tokens of one frame of the block; keys: the
+    // rows [h_min - r, h_max + r] of every window frame (one contiguous run
+    // of tokens per frame), narrowed per query by the neighbourhood mask.
+    const int f = blockIdx.x / p.tiles_per_frame, t0 = (blockIdx.x % p.tiles_per_frame) * (QT * BM);
+    it.head = blockIdx.y;
+    it.kind = ITEM_PROXY;
+    it.q0 = f * g.F + t0;
+    it.nq = min(QT * BM, g.F - t0);
+    it.out_plane = 3;
+    it.k_row0 = 0;
+    const int hmin = t0 / g.Fw, hmax = (t0 + it.nq - 1) / g.Fw;
+    it.rlo = max(0, hmin - g.radius);
+    it.rlen = (min(g.Fh - 1, hmax + g.radius) - it.rlo + 1) * g.Fw;
+    it.tpf = (it.rlen + BN - 1) / BN;
+    it.k_len = p.proxy_frames * it.tpf * BN;
+  } else if (p.item_mode == ITEMS_LIST) {
     const WorkItem w = p.items[blockIdx.x];
     it.head = w.head;
     it.kind = w.kind;
@@ -301,7 +322,7 @@ __device__ __forceinline__ int tc_query_token(const TcItem& it, const Geom& g, i
 
 // ---------------------------------------------------------------- the kernel
 
-template <int D>
+template <int D, bool PROXY>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ TcArgs args) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -384,7 +405,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       for (int t = 0; t < n_tiles; ++t) {
         const int st = t % STAGES;
         const uint32_t wpar = ((t / STAGES) - 1) & 1;
-        const int row = (int)(it.k_row0 + (int64_t)t * BN);
+        int row;
+        if (PROXY) {
+          const int f = t / it.tpf;
+          row = f * g.F + it.rlo * g.Fw + (t - f * it.tpf) * BN;
+        } else {
+          row = (int)(it.k_row0 + (int64_t)t * BN);
+        }
         if (t >= STAGES && !mbar_wait_bounded(bar(B_KEMPTY + st), wpar, abort_flag, WAIT_LIMIT_NS)) break;
         mbar_expect_tx(bar(B_KFULL + st), L::KV_BYTES);
 #pragma unroll
@@ -499,6 +526,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     const float sl2 = g.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
+    int hq = 0, wq = 0;   // PROXY: this row's query position in its frame
+    if (PROXY) {
+      const int pos = (it.q0 + qrow) % g.F;
+      hq = pos / g.Fw;
+      wq = pos - hq * g.Fw;
+    }
     auto wait_warp = [&](int slot, uint32_t parity) -> bool {
       const bool w = mbar_wait_bounded(bar(slot), parity, abort_flag, WAIT_LIMIT_NS);
       return __all_sync(0xffffffffu, w);
@@ -507,7 +540,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       if (!wait_warp(B_SFULL + grp, j & 1)) { ok = false; break; }
       tc_fence_after();
       const int valid = min(BN, it.k_len - j * BN);
-      const bool full = valid == BN;   // only a key run's last tile is partial
+      const bool full = PROXY || valid == BN;   // only a key run's last tile is partial
+      // PROXY: bit e of mw[e / 32] marks key column e of this tile as inside
+      // the row's (2r+1) x (2r+1) neighbourhood (at most 2r+1 runs of at most
+      // 2r+1 keys; the band's rows are consecutive frame rows).
+      uint32_t mw[BN / 32];
+#pragma unroll
+      for (int w = 0; w < BN / 32; ++w) mw[w] = 0u;
+      if (PROXY) {
+        const int o = (j % it.tpf) * BN;
+        const int rhi = it.rlo + it.rlen / g.Fw - 1;
+        const int c_lo = max(0, wq - g.radius), c_hi = min(g.Fw - 1, wq + g.radius);
+        for (int hk = max(it.rlo, hq - g.radius); hk <= min(rhi, hq + g.radius); ++hk) {
+          const int a = max((hk - it.rlo) * g.Fw + c_lo - o, 0);
+          const int b = min((hk - it.rlo) * g.Fw + c_hi - o, BN - 1);
+#pragma unroll
+          for (int w = 0; w < BN / 32; ++w) {
+            const int lo = max(a, 32 * w), hi = min(b, 32 * w + 31);
+            if (lo <= hi) mw[w] |= (uint32_t)(((1ull << (hi - lo + 1)) - 1ull) << (lo - 32 * w));
+          }
+        }
+      }
       // Pass 1: row max over the tile (8 independent partial maxima,
       // three-input max).
       float pm[8];
@@ -518,7 +571,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         uint32_t x[32];
         tmem_ld32(t_s + c * 32, x);
         tmem_wait_ld();
-        if (!full) {
+        if (PROXY) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (!((mw[c] >> e) & 1u)) x[e] = __float_as_uint(-INFINITY);
+        } else if (!full) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (c * 32 + e >= valid) x[e] = __float_as_uint(-INFINITY);
@@ -538,7 +595,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       } else if (__any_sync(0xffffffffu, m_new > m_run + RESCALE_LOG2)) {
         // O_i holds P_i(0..j-1) V, all of it complete (the commit that
         // signalled S_i(j) covers it): scale this warp's rows to the new max.
-        const float alpha = ex2(m_run - m_new);
+        // (A row still without any unmasked key keeps m = -inf and alpha 1.)
+        const float alpha = m_new == -INFINITY ? 1.f : ex2(m_run - m_new);
         l_run *= alpha;
         m_run = m_new;
 #pragma unroll
@@ -555,7 +613,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       // Pass 2: probabilities 2^(s*scale*log2e - m), 64 keys at a time,
       // packed two per column into P_i.  Masked keys become -inf, whose
       // exponent is 0.
-      const float neg_m = -m_run;
+      // A row whose keys have all been masked so far keeps m = -inf; its
+      // probabilities are all 0 (exponent of -inf), not NaN.
+      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
       float ps[8];   // 4 independent pairs of partial sums
 #pragma unroll
       for (int u = 0; u < 8; ++u) ps[u] = 0.f;
@@ -567,7 +627,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         tmem_ld32(t_s + h * 64, x);
         tmem_ld32(t_s + h * 64 + 32, x + 32);
         tmem_wait_ld();
-        if (!full) {
+        if (PROXY) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (!((mw[2 * h + e / 32] >> (e & 31)) & 1u)) x[e] = __float_as_uint(-INFINITY);
+        } else if (!full) {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
             if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
@@ -676,17 +740,17 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D>
+template <int D, bool PROXY>
 cudaError_t launch_d(const TcArgs& a, dim3 grid, cudaStream_t s) {
   constexpr int smem = Layout<D>::ALLOC;
   static_assert(smem <= 232448, "shared memory budget");
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attr = cudaFuncSetAttribute(attn_tc_kernel<D, PROXY>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr != cudaSuccess) return attr;
-  attn_tc_kernel<D><<<grid, NTHREADS, smem, s>>>(a);
+  attn_tc_kernel<D, PROXY><<<grid, NTHREADS, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -705,7 +769,9 @@ cudaError_t launch_attention_tc(const AttnParams& p, const TcKV& kv, dim3 grid, 
   if ((e = make_map(&a.tv, kv.v, p.g.d, kv.heads, kv.rows)) != cudaSuccess) return e;
   a.p = p;
   a.kv_head_coord = kv.heads > 1 ? 1 : 0;
-  return p.g.d == 128 ? launch_d<128>(a, grid, s) : launch_d<64>(a, grid, s);
+  if (p.item_mode == ITEMS_PROXY)
+    return p.g.d == 128 ? launch_d<128, true>(a, grid, s) : launch_d<64, true>(a, grid, s);
+  return p.g.d == 128 ? launch_d<128, false>(a, grid, s) : launch_d<64, false>(a, grid, s);
 }
 
 }  // namespace hc
