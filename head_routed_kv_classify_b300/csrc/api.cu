@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -128,9 +129,8 @@ hc_status check_labels(const hc_config* cfg, const int8_t* labels) {
   return HC_OK;
 }
 
-// Cache layout and the routed work list.  Items are ordered by decreasing
-// work so that the hardware block scheduler approximates
-// longest-processing-time-first.
+// Cache layout and the routed work list.  The hardware block scheduler
+// dispatches items in list order.
 void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
   const Geom g = make_geom(cfg);
   const int BM = hc::attention_block_rows(cfg.dtype, cfg.head_dim);
@@ -175,12 +175,27 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
         }
     }
   }
+  // Order: groups of items that read the same key run (one head's block or
+  // window run, or one Spatial cell of one head) stay adjacent, so that the
+  // CTAs sharing a run execute together and all but the first read it from
+  // L2; groups go longest-first (by their total work) and, inside a group,
+  // items go longest-first.
   auto cost = [&](const WorkItem& w) {
     const int64_t keys = w.k_per_frame > 0 ? (int64_t)w.k_per_frame * g.Wf : w.k_len;
     return keys * w.nq;
   };
-  std::stable_sort(P.items.begin(), P.items.end(),
-                   [&](const WorkItem& x, const WorkItem& y) { return cost(x) > cost(y); });
+  auto group = [&](const WorkItem& w) -> int64_t {
+    return (int64_t)w.head * (1 << 20) + (w.kind == hc::ITEM_CELL ? w.cell + 1 : 0);
+  };
+  std::map<int64_t, int64_t> group_cost;
+  for (const WorkItem& w : P.items) group_cost[group(w)] += cost(w);
+  std::stable_sort(P.items.begin(), P.items.end(), [&](const WorkItem& x, const WorkItem& y) {
+    const int64_t gx = group(x), gy = group(y);
+    const int64_t cx = group_cost[gx], cy = group_cost[gy];
+    if (cx != cy) return cx > cy;
+    if (gx != gy) return gx < gy;
+    return cost(x) > cost(y);
+  });
   const size_t row_bytes = (size_t)g.d * esize_of(cfg.dtype);
   P.off_items = 256;
   P.off_k = round_up(P.off_items + P.items.size() * sizeof(WorkItem), 256);
