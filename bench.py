@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="720p", choices=["480p", "720p", "1080p", "rollout"])
+    ap.add_argument("--workload", default="720p", choices=["480p", "720p", "1080p", "rollout", "sweep", "agreement", "stability"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -429,6 +429,215 @@ def run_rollout(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- threshold sweep
+
+def run_sweep(args, rank, world, local_rank):
+    """The FPS side of the threshold ablation (Figure 5 caption of the Pith
+    review of HeadCast): on the planted 720P layer, classify with theta (all
+    three cosine gates) over a grid at theta_sc = 0.755, and with theta_sc over
+    a grid at theta = 0.95; for each setting, the archetype mix the classifier
+    picks, the steady-state cache bytes, the routed-attention time and its
+    speedup over full attention.  (The quality side needs a trained model.)"""
+    import torch
+    import head_routed_kv_classify_b300 as hc
+    from head_routed_kv_classify_b300 import build as hcb
+
+    if not os.path.exists(hc.LIB_PATH):
+        hcb.build()
+    hc.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    shape = synth.SHAPES["720p"]
+    inp = synth.make_layer(shape, seed=shape.seed + 1000 * rank)
+
+    def to_dev(x):
+        return torch.from_numpy(x.raw.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+
+    q, k, v = to_dev(inp.q), to_dev(inp.k), to_dev(inp.v)
+    o = torch.empty_like(q)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def timed(fn, reps):
+        evs = []
+        for i in range(reps + 3):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            if i >= 3:
+                evs.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.mean(x.elapsed_time(y) for x, y in evs)
+
+    base = hc.config_for(shape)
+    full_ms = timed(lambda: hc.hc_full_attention(base, q, k, v, o=o), 5)
+    # The planted heads clear their gates by wide margins, so theta has to
+    # come down to where unplanted (Global) heads' similarities lie before
+    # the mix, and with it the FPS side, moves.
+    grid = [(t, 0.755) for t in (0.20, 0.30, 0.40, 0.50, 0.60, 0.70, 0.80, 0.90, 0.95, 0.99)]
+    grid += [(0.95, sc) for sc in (0.50, 0.70, 0.85, 0.95, 0.99)]
+    rows = []
+    for theta, theta_sc in grid:
+        cfg = hc.config_for(shape, theta_sink=theta, theta_dummy=theta, theta_spatial=theta,
+                            theta_score=theta_sc)
+        labels, _, _ = hc.hc_classify(cfg, q, k, v)
+        cache = hc.hc_cache_create(cfg, labels, device=dev)
+        cache.restructure(k, v, 0)
+        ms = timed(lambda: cache.routed_attention(q, o), 10)
+        rows.append({"theta": theta, "theta_sc": theta_sc,
+                     "mix": "".join("SDPG"[int(a)] for a in labels),
+                     "routed_ms": ms, "speedup_vs_full": full_ms / ms,
+                     "cache_bytes": cache.info()["bytes"]})
+        cache.close()
+    hc.hc_get_last_error()
+    if rank != 0:
+        return
+    at_default = [r for r in rows if r["theta"] == 0.95 and r["theta_sc"] == 0.755][0]
+    line = {"metric": METRIC, "value": shape.n_q / (at_default["routed_ms"] * 1e-3), "unit": UNIT,
+            "n_gpus": world, "steps": 10, "warmup": 3, "ms_per_step": at_default["routed_ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) Q/K/V with planted archetypes; 720P shapes)",
+            "config": {"workload": "720p threshold sweep", "planted_mix": "".join("SDPG"[a] for a in shape.mix),
+                       "l2": "flushed before every launch (512 MB write)"},
+            "full_attention_ms": full_ms, "sweep": rows}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- proxy vs deployed
+
+def run_agreement(args, rank, world, local_rank):
+    """How well the classifier's Spatial proxy (the (2r+1)x(2r+1)
+    neighbourhood, r = 2) stands for the deployed path (the query's 10x10
+    cell), the comparison the Pith review of HeadCast asks for (major comment
+    2): every layer is classified twice, once with each proxy, and the line
+    reports per head c_spatial, P5, MSE and score under both, and how many
+    labels agree.  Layers: the planted 720P layer and the first six layers of
+    the 30-layer rollout mix."""
+    import torch
+    import head_routed_kv_classify_b300 as hc
+    from head_routed_kv_classify_b300 import build as hcb
+
+    if not os.path.exists(hc.LIB_PATH):
+        hcb.build()
+    hc.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    shape = synth.SHAPES["720p"]
+    R = synth.ROLLOUT_720P
+    mixes = [tuple(shape.mix)] + [tuple(int(a) for a in m) for m in synth.rollout_mix(R["layers"], shape.n_heads, R["seed"])[:6]]
+
+    def to_dev(x):
+        return torch.from_numpy(x.raw.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+
+    layers, agree, total, t_ms = [], 0, 0, []
+    for n, mix in enumerate(mixes):
+        inp = synth.make_layer(shape, seed=(shape.seed if n == 0 else R["seed"] * 100 + n - 1) + 1000 * rank, mix=mix)
+        q, k, v = to_dev(inp.q), to_dev(inp.k), to_dev(inp.v)
+        out = {}
+        for mode, name in ((hc.HC_PROXY_NEIGHBOURHOOD, "neighbourhood"), (hc.HC_PROXY_CELL, "cell")):
+            cfg = hc.config_for(shape, proxy_mode=mode)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            labels, _, stats = hc.hc_classify(cfg, q, k, v)
+            b.record()
+            torch.cuda.synchronize()
+            t_ms.append((name, a.elapsed_time(b)))
+            out[name] = (labels, stats.cpu().numpy())
+        ln, sn = out["neighbourhood"]
+        lc, sc = out["cell"]
+        agree += int(np.sum(ln == lc))
+        total += len(ln)
+        layers.append({"planted": "".join("SDPG"[a] for a in mix),
+                       "labels_neighbourhood": "".join("SDPG"[int(a)] for a in ln),
+                       "labels_cell": "".join("SDPG"[int(a)] for a in lc),
+                       "c_spatial": [[round(float(x), 4), round(float(y), 4)] for x, y in zip(sn[:, 2], sc[:, 2])],
+                       "p5": [[round(float(x), 4), round(float(y), 4)] for x, y in zip(sn[:, 3], sc[:, 3])],
+                       "score": [[round(float(x), 4), round(float(y), 4)] for x, y in zip(sn[:, 5], sc[:, 5])]})
+    hc.hc_get_last_error()
+    if rank != 0:
+        return
+    cls_ms = statistics.mean(t for nm, t in t_ms if nm == "neighbourhood")
+    line = {"metric": METRIC, "value": None, "unit": UNIT, "n_gpus": world, "steps": len(mixes),
+            "warmup": 0, "ms_per_step": cls_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) Q/K/V with planted archetypes; 720P shapes)",
+            "config": {"workload": "720p proxy vs deployed Spatial agreement", "layers": len(mixes),
+                       "stat_pairs": "[neighbourhood proxy, deployed cell] per head"},
+            "label_agreement": agree / total, "heads": total,
+            "classify_ms": {nm: statistics.mean(t for m, t in t_ms if m == nm) for nm in ("neighbourhood", "cell")},
+            "layers": layers}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- stability
+
+def run_stability(args, rank, world, local_rank):
+    """Re-classification stability on synthetic streams (the pages report the
+    share of identical archetypes across AR steps; Pith review of HeadCast,
+    "Core claim" / major comment 1).  A 480P-shaped layer (2/3/4/3 planted
+    heads) streams 13 blocks whose planted structure persists; after the
+    window first fills (block 6) a fraction `drift` of each planted query
+    term is replaced by an unrelated one.  The layer is classified at block 6
+    and again at blocks 7, 9 and 12, each time over the Sink block plus the
+    six newest blocks, and the line reports the share of heads whose label is
+    unchanged, per drift level.  (The timestep axis needs a diffusion model.)"""
+    import torch
+    import head_routed_kv_classify_b300 as hc
+    from head_routed_kv_classify_b300 import build as hcb
+
+    if not os.path.exists(hc.LIB_PATH):
+        hcb.build()
+    hc.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    shape = synth.SHAPES["480p"]
+    cfg = hc.config_for(shape)
+    fill = shape.blocks_per_window - 1
+    checks = (fill + 1, fill + 3, fill + 6)
+
+    def to_dev(x):
+        return torch.from_numpy(x.raw.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+
+    results = []
+    for drift in (0.0, 0.3, 0.6):
+        blocks = synth.make_stream(shape, seed=shape.seed + 500 + 1000 * rank, n_blocks=checks[-1] + 1,
+                                   drift=drift)
+        dq = [to_dev(b[0]) for b in blocks]
+        dk = [to_dev(b[1]) for b in blocks]
+        dv = [to_dev(b[2]) for b in blocks]
+
+        def classify_at(b):
+            ids = [0] + list(range(b - shape.blocks_per_window + 2, b + 1))
+            k = torch.cat([dk[i] for i in ids])
+            v = torch.cat([dv[i] for i in ids])
+            labels, _, _ = hc.hc_classify(cfg, dq[b], k, v)
+            return labels
+
+        first = classify_at(fill)
+        row = {"drift": drift, "labels_at_fill": "".join("SDPG"[int(a)] for a in first),
+               "planted": "".join("SDPG"[a] for a in shape.mix), "later": []}
+        for b in checks:
+            lab = classify_at(b)
+            row["later"].append({"block": b, "labels": "".join("SDPG"[int(a)] for a in lab),
+                                 "identical": float(np.mean(lab == first))})
+        row["identical_mean"] = float(np.mean([x["identical"] for x in row["later"]]))
+        results.append(row)
+        del dq, dk, dv, blocks
+    hc.hc_get_last_error()
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": None, "unit": UNIT, "n_gpus": world, "steps": len(checks),
+            "warmup": 0, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded streams with persistent planted archetypes and query drift; 480P shapes)",
+            "config": {"workload": "480p re-classification stability",
+                       "window_at_block_b": "block 0 (Sink) + blocks b-5..b"},
+            "stability": results}
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------------------- our arm
 
 def run_ours(args, shape, rank, world, local_rank):
@@ -622,6 +831,7 @@ def run_ours(args, shape, rank, world, local_rank):
                                 (total_ms / args.steps),
         "classify_ms": classify_ms, "restructure_ms": restructure_ms,
         "paths": paths,
+        "memory": hc.memory_report(cfg, labels),
         "wall_s_timed": wall,
     }
     if not args.no_cpu_baseline:
@@ -634,7 +844,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    shape = synth.SHAPES[args.workload if args.workload != "rollout" else "720p"]
+    shape = synth.SHAPES[args.workload if args.workload in synth.SHAPES else "720p"]
     if args.impl == "reference":
         run_reference(args, shape, rank, world)
         return
@@ -645,6 +855,12 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     if args.workload == "rollout":
         run_rollout(args, rank, world, local_rank)
+    elif args.workload == "sweep":
+        run_sweep(args, rank, world, local_rank)
+    elif args.workload == "agreement":
+        run_agreement(args, rank, world, local_rank)
+    elif args.workload == "stability":
+        run_stability(args, rank, world, local_rank)
     else:
         run_ours(args, shape, rank, world, local_rank)
     if world > 1:

@@ -11,6 +11,10 @@ Names mirror the C ABI in include/headcast.h:
     hc_classify, hc_cache_bytes, hc_cache_create (-> Cache),
     hc_cache_restructure, hc_cache_append, hc_routed_attention,
     hc_full_attention, hc_get_last_error, hc_classify_static_scratch
+
+Host-side helpers (no device work): memory_report (steady-state cache bytes
+against the monolithic window), save_labels / load_labels (per-layer
+archetype labels as text).
 """
 from __future__ import annotations
 
@@ -25,10 +29,12 @@ LIB_PATH = os.path.join(_PKG, "libheadcast.so")
 SINK, DUMMY, SPATIAL, GLOBAL = 0, 1, 2, 3
 ARCHETYPES = ("sink", "dummy", "spatial", "global")
 HC_BF16, HC_FP32 = 0, 1
+HC_PROXY_NEIGHBOURHOOD, HC_PROXY_CELL = 0, 1
 STATUS_NAMES = {0: "HC_OK", 1: "HC_ERR_INVALID_ARG", 2: "HC_ERR_SHAPE", 3: "HC_ERR_DTYPE",
                 4: "HC_ERR_ALIGN", 5: "HC_ERR_STATE", 6: "HC_ERR_CUDA", 7: "HC_ERR_TIMEOUT",
                 8: "HC_ERR_UNSUPPORTED", 9: "HC_ERR_SIZE"}
 MAX_HEADS = 64
+ABI_VERSION = 2                   # HC_ABI_VERSION this binding is written against
 STATIC_SCRATCH_BYTES = 16 << 20   # HC_STATIC_SCRATCH_BYTES
 
 # Every symbol include/headcast.h declares.
@@ -56,7 +62,8 @@ class HcConfig(C.Structure):
                 ("window_frames", C.c_int32), ("dtype", C.c_int32), ("softmax_scale", C.c_float),
                 ("theta_sink", C.c_float), ("theta_dummy", C.c_float),
                 ("theta_spatial", C.c_float), ("theta_score", C.c_float), ("gamma", C.c_float),
-                ("proxy_radius", C.c_int32), ("cell_h", C.c_int32), ("cell_w", C.c_int32)]
+                ("proxy_radius", C.c_int32), ("cell_h", C.c_int32), ("cell_w", C.c_int32),
+                ("proxy_mode", C.c_int32)]
 
     @property
     def F(self):
@@ -110,6 +117,8 @@ def load(path: str = LIB_PATH):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
+    if lib.hc_abi_version() != ABI_VERSION:
+        raise HeadcastUnavailable(f"{path} has ABI {lib.hc_abi_version()}, binding expects {ABI_VERSION}")
     _lib = lib
     return lib
 
@@ -339,3 +348,64 @@ def hc_full_attention(cfg, q, k, v, o=None, n_key_frames=None, stream=None):
 
 def hc_get_last_error(stream=None):
     _check(load().hc_get_last_error(_stream(stream)))
+
+
+# ----------------------------------------------------------------- host-side helpers
+
+def memory_report(cfg, labels) -> dict:
+    """Steady-state KV-cache footprint of one layer for these labels against
+    the monolithic [window][H][d] K/V cache, from hc_cache_bytes (host only).
+    [Pith review of HeadCast, Figure 9 caption / Appendix C: memory of the
+    restructured cache.]"""
+    lab = np.asarray(labels, dtype=np.int8)
+    esize = 2 if cfg.dtype == HC_BF16 else 4
+    F, d = cfg.F, cfg.head_dim
+    rows = {ARCHETYPES[a]: 0 for a in range(4)}
+    for a in lab:
+        rows[ARCHETYPES[int(a)]] += (cfg.frames_per_block if a in (SINK, DUMMY) else cfg.window_frames) * F
+    total = hc_cache_bytes(cfg, lab)
+    mono = 2 * cfg.window_frames * F * cfg.n_heads * d * esize
+    return {"bytes": total, "kv_bytes": 2 * sum(rows.values()) * d * esize, "monolithic_bytes": mono,
+            "ratio": total / mono, "rows_by_archetype": rows}
+
+
+_LETTERS = "SDPG"
+
+
+def save_labels(path, labels):
+    """Write per-layer archetype labels ([layers][heads] ints 0..3) as text:
+    a comment line, then one line per layer: the layer index and one letter
+    per head (S Sink, D Dummy, P Spatial, G Global)."""
+    lab = np.atleast_2d(np.asarray(labels, dtype=np.int64))
+    if lab.size == 0 or lab.min() < 0 or lab.max() > 3:
+        raise ValueError("labels must be archetypes 0..3")
+    with open(path, "w") as f:
+        f.write(f"# headcast head archetypes: {lab.shape[0]} layers x {lab.shape[1]} heads; "
+                "S=Sink D=Dummy P=Spatial G=Global\n")
+        for layer, row in enumerate(lab):
+            f.write(f"{layer} {''.join(_LETTERS[int(a)] for a in row)}\n")
+
+
+def load_labels(path) -> np.ndarray:
+    """Read labels written by save_labels: int8 [layers][heads].  Raises
+    ValueError on a malformed file (unknown letter, ragged rows, layers out
+    of order or missing)."""
+    rows = []
+    with open(path) as f:
+        for n, line in enumerate(f, 1):
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            if len(parts) != 2 or not parts[0].isdigit():
+                raise ValueError(f"{path}:{n}: expected '<layer> <letters>'")
+            if int(parts[0]) != len(rows):
+                raise ValueError(f"{path}:{n}: layer {parts[0]} out of order (expected {len(rows)})")
+            if any(c not in _LETTERS for c in parts[1]):
+                raise ValueError(f"{path}:{n}: unknown archetype letter in {parts[1]!r}")
+            if rows and len(parts[1]) != len(rows[0]):
+                raise ValueError(f"{path}:{n}: {len(parts[1])} heads, earlier layers have {len(rows[0])}")
+            rows.append([_LETTERS.index(c) for c in parts[1]])
+    if not rows:
+        raise ValueError(f"{path}: no layers")
+    return np.array(rows, dtype=np.int8)

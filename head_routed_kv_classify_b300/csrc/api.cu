@@ -79,6 +79,7 @@ Geom make_geom(const hc_config& c) {
   g.ncell_h = hc::n_cells(c.frame_h, c.cell_h);
   g.ncell_w = hc::n_cells(c.frame_w, c.cell_w);
   g.radius = c.proxy_radius;
+  g.proxy_mode = c.proxy_mode;
   const double scale = c.softmax_scale > 0.f ? (double)c.softmax_scale : 1.0 / std::sqrt((double)c.head_dim);
   g.scale_log2 = (float)(scale * 1.4426950408889634);
   return g;
@@ -282,6 +283,8 @@ hc_status hc_config_validate(const hc_config* c) {
     return fail(HC_ERR_INVALID_ARG, "non-finite threshold or negative scale");
   if (c->proxy_radius < 0 || c->cell_h < 1 || c->cell_w < 1)
     return fail(HC_ERR_INVALID_ARG, "proxy_radius %d / cell %dx%d", c->proxy_radius, c->cell_h, c->cell_w);
+  if (c->proxy_mode != HC_PROXY_NEIGHBOURHOOD && c->proxy_mode != HC_PROXY_CELL)
+    return fail(HC_ERR_INVALID_ARG, "proxy_mode %d is not 0 or 1", c->proxy_mode);
   return HC_OK;
 }
 

@@ -73,8 +73,9 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p) {
     it.k_row0 = 0;
     int hmin = (t * kBM) / g.Fw;
     int hmax = (t * kBM + it.nq - 1) / g.Fw;
-    it.rlo = max(0, hmin - g.radius);
-    int rhi = min(g.Fh - 1, hmax + g.radius);
+    int lo, hi, wl, wh, rhi;
+    proxy_window(g, hmin, 0, it.rlo, hi, wl, wh);
+    proxy_window(g, hmax, 0, lo, rhi, wl, wh);
     it.range_len = (rhi - it.rlo + 1) * g.Fw;
     it.tpr = (it.range_len + BN - 1) / BN;
     it.k_len = p.proxy_frames * it.range_len;
@@ -135,11 +136,11 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnParams p) {
     const int tok = query_token(it, g, r);
     for (int c = lane; c < D; c += 32) sq[warp][c] = Q[tok * HD + it.head * D + c];
     __syncwarp();
-    int hq = 0, wq = 0;
+    int h_lo = 0, h_hi = 0, w_lo = 0, w_hi = 0;
     if (it.kind == ITEM_PROXY) {
-      int tp = tok % g.F;
-      hq = tp / g.Fw;
-      wq = tp - hq * g.Fw;
+      const int tp = tok % g.F;
+      const int hq = tp / g.Fw;
+      proxy_window(g, hq, tp - hq * g.Fw, h_lo, h_hi, w_lo, w_hi);
     }
     float m = -CUDART_INF_F, l = 0.f, acc[PER];
 #pragma unroll
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnParams p) {
       if (ok && it.kind == ITEM_PROXY) {
         int pos = pos0 + lane;
         int hk = pos / g.Fw, wk = pos - hk * g.Fw;
-        ok = abs(hk - hq) <= g.radius && abs(wk - wq) <= g.radius;
+        ok = hk >= h_lo && hk <= h_hi && wk >= w_lo && wk <= w_hi;
       }
       float x = -CUDART_INF_F;
       if (ok) {

@@ -278,8 +278,10 @@ __device__ __forceinline__ TcItem tc_decode(const AttnParams& p) {
     it.out_plane = 3;
     it.k_row0 = 0;
     const int hmin = t0 / g.Fw, hmax = (t0 + it.nq - 1) / g.Fw;
-    it.rlo = max(0, hmin - g.radius);
-    it.rlen = (min(g.Fh - 1, hmax + g.radius) - it.rlo + 1) * g.Fw;
+    int lo, rhi, wl, wh;
+    proxy_window(g, hmin, 0, it.rlo, rhi, wl, wh);
+    proxy_window(g, hmax, 0, lo, rhi, wl, wh);
+    it.rlen = (rhi - it.rlo + 1) * g.Fw;
     it.tpf = (it.rlen + BN - 1) / BN;
     it.k_len = p.proxy_frames * it.tpf * BN;
   } else if (p.item_mode == ITEMS_LIST) {
@@ -526,11 +528,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     const float sl2 = g.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    int hq = 0, wq = 0;   // PROXY: this row's query position in its frame
+    int h_lo = 0, h_hi = -1, w_lo = 0, w_hi = -1;   // PROXY: this row's key window in a frame
     if (PROXY) {
       const int pos = (it.q0 + qrow) % g.F;
-      hq = pos / g.Fw;
-      wq = pos - hq * g.Fw;
+      const int hq = pos / g.Fw;
+      proxy_window(g, hq, pos - hq * g.Fw, h_lo, h_hi, w_lo, w_hi);
     }
     auto wait_warp = [&](int slot, uint32_t parity) -> bool {
       const bool w = mbar_wait_bounded(bar(slot), parity, abort_flag, WAIT_LIMIT_NS);
@@ -542,18 +544,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       const int valid = min(BN, it.k_len - j * BN);
       const bool full = PROXY || valid == BN;   // only a key run's last tile is partial
       // PROXY: bit e of mw[e / 32] marks key column e of this tile as inside
-      // the row's (2r+1) x (2r+1) neighbourhood (at most 2r+1 runs of at most
-      // 2r+1 keys; the band's rows are consecutive frame rows).
+      // the row's proxy window (one run of keys per window row; the band's
+      // rows are consecutive frame rows).
       uint32_t mw[BN / 32];
 #pragma unroll
       for (int w = 0; w < BN / 32; ++w) mw[w] = 0u;
       if (PROXY) {
         const int o = (j % it.tpf) * BN;
         const int rhi = it.rlo + it.rlen / g.Fw - 1;
-        const int c_lo = max(0, wq - g.radius), c_hi = min(g.Fw - 1, wq + g.radius);
-        for (int hk = max(it.rlo, hq - g.radius); hk <= min(rhi, hq + g.radius); ++hk) {
-          const int a = max((hk - it.rlo) * g.Fw + c_lo - o, 0);
-          const int b = min((hk - it.rlo) * g.Fw + c_hi - o, BN - 1);
+        for (int hk = max(it.rlo, h_lo); hk <= min(rhi, h_hi); ++hk) {
+          const int a = max((hk - it.rlo) * g.Fw + w_lo - o, 0);
+          const int b = min((hk - it.rlo) * g.Fw + w_hi - o, BN - 1);
 #pragma unroll
           for (int w = 0; w < BN / 32; ++w) {
             const int lo = max(a, 32 * w), hi = min(b, 32 * w + 31);

@@ -22,6 +22,7 @@ struct Geom {
   int H, d, Fh, Fw, F, fpb, Wf, blk;   // blk = fpb * F (tokens per block)
   int cell_h, cell_w, ncell_h, ncell_w;
   int radius;
+  int proxy_mode;                      // HC_PROXY_NEIGHBOURHOOD or HC_PROXY_CELL
   float scale_log2;                    // softmax scale * log2(e)
 };
 
@@ -42,6 +43,27 @@ HC_HD int cell_extent(int i, int n, int c, int nc) {
 HC_HD int cell_tokens_before(const Geom& g, int ci, int cj) {
   int hz = cell_extent(ci, g.Fh, g.cell_h, g.ncell_h);
   return ci * g.cell_h * g.Fw + hz * cj * g.cell_w;
+}
+
+// Rows [h_lo, h_hi] and columns [w_lo, w_hi] of the classification proxy of
+// a query at (h, w): the clipped (2r+1) x (2r+1) neighbourhood, or with
+// HC_PROXY_CELL the query's deployed cell.  Both bounds are non-decreasing in
+// h and in w, so the band of rows of a run of queries is [h_lo(first row),
+// h_hi(last row)].
+// [Pith review of HeadCast, major comment 2: proxy r = 2 vs deployed cells.]
+HC_HD void proxy_window(const Geom& g, int h, int w, int& h_lo, int& h_hi, int& w_lo, int& w_hi) {
+  if (g.proxy_mode == HC_PROXY_CELL) {
+    const int ci = cell_index(h, g.cell_h, g.ncell_h), cj = cell_index(w, g.cell_w, g.ncell_w);
+    h_lo = ci * g.cell_h;
+    h_hi = h_lo + cell_extent(ci, g.Fh, g.cell_h, g.ncell_h) - 1;
+    w_lo = cj * g.cell_w;
+    w_hi = w_lo + cell_extent(cj, g.Fw, g.cell_w, g.ncell_w) - 1;
+  } else {
+    h_lo = h - g.radius < 0 ? 0 : h - g.radius;
+    h_hi = h + g.radius > g.Fh - 1 ? g.Fh - 1 : h + g.radius;
+    w_lo = w - g.radius < 0 ? 0 : w - g.radius;
+    w_hi = w + g.radius > g.Fw - 1 ? g.Fw - 1 : w + g.radius;
+  }
 }
 
 // Work item kinds.

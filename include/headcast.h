@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define HC_ABI_VERSION 1
+#define HC_ABI_VERSION 2
 #define HC_MAX_HEADS 64
 
 typedef enum { HC_SINK = 0, HC_DUMMY = 1, HC_SPATIAL = 2, HC_GLOBAL = 3 } hc_archetype;
@@ -93,7 +93,14 @@ typedef struct {
   int32_t proxy_radius;     /* r of the (2r+1)x(2r+1) classification proxy   */
   int32_t cell_h;           /* deployed Spatial cell height (10)              */
   int32_t cell_w;           /* deployed Spatial cell width (10)               */
+  int32_t proxy_mode;       /* Spatial proxy of the classifier:
+                               HC_PROXY_NEIGHBOURHOOD (0, the paper's) = the
+                               clipped (2r+1)x(2r+1) neighbourhood of the query;
+                               HC_PROXY_CELL (1) = the query's deployed cell
+                               (compares the proxy with the deployed path)    */
 } hc_config;
+
+typedef enum { HC_PROXY_NEIGHBOURHOOD = 0, HC_PROXY_CELL = 1 } hc_proxy_mode;
 
 typedef struct hc_cache hc_cache;   /* opaque host handle, one per layer */
 
@@ -119,7 +126,7 @@ const char* hc_last_error_message(void);
  * frames_per_block = 3, window_frames = 21, dtype = HC_BF16. */
 hc_status hc_config_default(hc_config* out);
 /* Check a config: H in 1..64, d in {64,128}, frame dims >= 1, window a
- * positive multiple of frames_per_block, finite thresholds. */
+ * positive multiple of frames_per_block, finite thresholds, proxy_mode 0/1. */
 hc_status hc_config_validate(const hc_config* cfg);
 
 /* ---------------------------------------------------------------------------
@@ -127,7 +134,8 @@ hc_status hc_config_validate(const hc_config* cfg);
  * step), each head's full-context output O_full is compared with its output
  * over (a) the window's first block (Sink proxy), (b) the window's last
  * block (Dummy proxy), (c) the (2r+1)x(2r+1) clipped neighbourhood of the
- * query's (h, w) in every window frame (Spatial proxy).  Per head:
+ * query's (h, w) in every window frame (Spatial proxy; with proxy_mode =
+ * HC_PROXY_CELL, the query's deployed cell instead).  Per head:
  *   c_x   = mean over the block's queries of cos(O_full, O_x),
  *   P5    = 5th percentile of cos(O_full, O_spatial) (linear interpolation
  *           at rank 0.05*(Nq-1)),

@@ -72,6 +72,10 @@ class Geometry:
     proxy_radius: int = 2          # r  [HC-pith Ledger "Spatial proxy radius r = 2"]
     cell_h: int = 10               # [HC-pith Ledger "deployed spatial grid cell = 10x10"]
     cell_w: int = 10
+    # Key set of the classifier's Spatial proxy: "neighbourhood" (the
+    # paper's (2r+1)x(2r+1) window) or "cell" (the deployed cell, to measure
+    # how well the proxy stands for the deployed path) [HC-pith major comment 2].
+    proxy_mode: str = "neighbourhood"
 
     @property
     def F(self):
@@ -295,7 +299,8 @@ def classification_outputs(q, k, v, geom: Geometry, head, scale=None, query_idx=
     o_full = attend_chunked(qh[qi], kh, vh, scale)
     o_sink = attend_chunked(qh[qi], kh[:blk], vh[:blk], scale)
     o_dummy = attend_chunked(qh[qi], kh[nk - blk:], vh[nk - blk:], scale)
-    o_sp = attend_by_position(qh, kh, vh, geom, n_frames, proxy_keys, scale, qi)
+    keyset = cell_keys if geom.proxy_mode == "cell" else proxy_keys
+    o_sp = attend_by_position(qh, kh, vh, geom, n_frames, keyset, scale, qi)
     return HeadProxies(o_full, o_sink, o_dummy, o_sp)
 
 

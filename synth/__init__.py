@@ -204,3 +204,56 @@ def make_block(shape: LayerShape, seed: int, mix=None, planted_dirs=None):
 def rollout_mix(layers: int, n_heads: int, seed: int) -> np.ndarray:
     """Per-(layer, head) archetypes drawn uniformly over the four."""
     return np.random.default_rng(seed).integers(0, 4, size=(layers, n_heads)).astype(np.int8)
+
+
+def make_stream(shape: LayerShape, seed: int, n_blocks: int, drift: float = 0.0,
+                drift_after: int | None = None, mix=None):
+    """One layer's blocks 0..n_blocks-1 with persistent planted structure
+    (Q, K, V per block, each a [3F][H][d] Tensor3).
+
+    Plants (directions from one generator seeded by ``seed``, noise per block
+    from a generator seeded by (seed, block)):
+      * Sink head: one direction u; every block's queries get c*u, block 0's
+        keys get 4*c*u;
+      * Dummy head: a fresh direction v_b per block; block b's queries get
+        c*v_b and its keys 4*c*v_b;
+      * Spatial head: one feature map s(h, w); queries get 4*a*s, keys a*s;
+      * Global head: none.
+    Drift: for blocks after ``drift_after`` (default: the block where the
+    window first fills), a fraction ``drift`` of each planted query term is
+    replaced by an unrelated one of the same norm (a fresh direction, or a
+    fresh feature map for Spatial heads), so the structure the classifier saw
+    weakens by that fraction."""
+    mix = tuple(shape.mix if mix is None else mix)
+    if drift_after is None:
+        drift_after = shape.blocks_per_window - 1
+    H, d, nq = shape.n_heads, shape.head_dim, shape.n_q
+    c = np.sqrt(3.0 * np.sqrt(d))
+    plant = np.random.default_rng(seed)
+    u = {h: random_unit(plant, d) for h in range(H) if mix[h] == SINK}
+    s = {h: spatial_features(plant, shape.frame_h, shape.frame_w, d) for h in range(H) if mix[h] == SPATIAL}
+    dummy_dirs = {h: [random_unit(plant, d) for _ in range(n_blocks)] for h in range(H) if mix[h] == DUMMY}
+    fresh_dirs = [[random_unit(plant, d) for _ in range(H)] for _ in range(n_blocks)]
+    fresh_maps = [{h: spatial_features(plant, shape.frame_h, shape.frame_w, d) for h in s} for _ in range(n_blocks)]
+    blocks = []
+    for b in range(n_blocks):
+        rng = np.random.default_rng([seed, b])
+        q = rng.standard_normal((nq, H, d), dtype=np.float32)
+        k = rng.standard_normal((nq, H, d), dtype=np.float32)
+        v = rng.standard_normal((nq, H, d), dtype=np.float32)
+        dl = drift if b > drift_after else 0.0
+        for h, arch in enumerate(mix):
+            if arch == SINK:
+                q[:, h, :] += (c * ((1 - dl) * u[h] + dl * fresh_dirs[b][h])).astype(np.float32)
+                if b == 0:
+                    k[:, h, :] += (4.0 * c * u[h]).astype(np.float32)
+            elif arch == DUMMY:
+                vb = dummy_dirs[h][b]
+                q[:, h, :] += (c * ((1 - dl) * vb + dl * fresh_dirs[b][h])).astype(np.float32)
+                k[:, h, :] += (4.0 * c * vb).astype(np.float32)
+            elif arch == SPATIAL:
+                sq = (1 - dl) * s[h] + dl * fresh_maps[b][h]
+                q[:, h, :] += np.tile(4.0 * c * sq, (shape.frames_per_block, 1)).astype(np.float32)
+                k[:, h, :] += np.tile(c * s[h], (shape.frames_per_block, 1)).astype(np.float32)
+        blocks.append((_store(q, shape.dtype), _store(k, shape.dtype), _store(v, shape.dtype)))
+    return blocks

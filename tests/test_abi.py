@@ -47,7 +47,7 @@ def test_library_does_not_need_libcuda(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.hc_abi_version() == 1
+    assert lib.hc_abi_version() == hc.ABI_VERSION == 2
     assert lib.hc_status_string(0) == b"ok"
     assert lib.hc_status_string(7) == b"device-side wait expired"
 
@@ -58,6 +58,7 @@ def test_config_default_holds_ledger_constants(lib):
     assert abs(cfg.theta_spatial - 0.95) < 1e-7 and abs(cfg.theta_score - 0.755) < 1e-7
     assert cfg.gamma == 5.0 and cfg.proxy_radius == 2 and (cfg.cell_h, cfg.cell_w) == (10, 10)
     assert cfg.frames_per_block == 3 and cfg.window_frames == 21
+    assert cfg.proxy_mode == hc.HC_PROXY_NEIGHBOURHOOD
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -66,6 +67,7 @@ def test_config_default_holds_ledger_constants(lib):
     ("window_frames", 20, "HC_ERR_SHAPE"), ("dtype", 7, "HC_ERR_DTYPE"),
     ("theta_sink", float("nan"), "HC_ERR_INVALID_ARG"), ("softmax_scale", -1.0, "HC_ERR_INVALID_ARG"),
     ("cell_w", 0, "HC_ERR_INVALID_ARG"), ("proxy_radius", -1, "HC_ERR_INVALID_ARG"),
+    ("proxy_mode", 2, "HC_ERR_INVALID_ARG"), ("proxy_mode", -1, "HC_ERR_INVALID_ARG"),
 ])
 def test_config_validation(lib, field, value, status):
     cfg = hc.make_config(12, 128, 45, 80)

@@ -28,8 +28,8 @@ SMALL = {
 STAT_ATOL = 2e-3
 
 
-def _run(shape, o_full=True):
-    cfg = hc.config_for(shape)
+def _run(shape, o_full=True, **cfg_overrides):
+    cfg = hc.config_for(shape, **cfg_overrides)
     inp = synth.make_layer(shape)
     q, k, v = (gu.to_dev(x, shape.dtype) for x in (inp.q, inp.k, inp.v))
     of = gu.torch().empty_like(q) if o_full else None
@@ -56,6 +56,19 @@ def test_classify_small(name):
     _compare_stats(stats, cls.stats, name)
     want_full = np.stack([o.o_full for o in cls.outputs], axis=1)
     gu.assert_close(of, want_full, shape.dtype, f"{name} o_full")
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_classify_cell_proxy_small(name):
+    """Classification with the deployed cell as the Spatial proxy (the
+    proxy-vs-deployed comparison): labels bit-exact and statistics against
+    the oracle run with the same proxy."""
+    shape = SMALL[name]
+    inp, labels, stats, _ = _run(shape, o_full=False, proxy_mode=hc.HC_PROXY_CELL)
+    geom = ref.geometry_of(shape, proxy_mode="cell")
+    cls = ref.classify(inp.q.values, inp.k.values, inp.v.values, geom)
+    assert list(labels) == list(cls.labels), (labels, cls.labels, cls.margins)
+    _compare_stats(stats, cls.stats, name + " cell proxy")
 
 
 def test_classify_480p():

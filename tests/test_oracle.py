@@ -330,3 +330,28 @@ def test_planted_tiny_recovered():
 @pytest.mark.slow
 def test_planted_480p_recovered():
     _check_planted(synth.SHAPES["480p"])
+
+
+def test_cell_proxy_mode_uses_the_deployed_cells():
+    """With the cell proxy the classifier's Spatial output is exactly the
+    deployed Spatial path's output (the same key sets), and a cell covering
+    the grid turns it into the full-context output."""
+    shape = synth.custom_shape("cellproxy", n_heads=2, head_dim=16, frame_h=13, frame_w=11,
+                               window_frames=6, dtype="fp32", seed=21, mix=(2, 3))
+    inp = synth.make_layer(shape)
+    q, k, v = inp.q.values, inp.k.values, inp.v.values
+    geom = ref.geometry_of(shape, proxy_mode="cell")
+    cache = ref.CacheModel(geom)
+    blk = shape.n_q
+    for b in range(shape.blocks_per_window):
+        cache.put(b, k[b * blk:(b + 1) * blk], v[b * blk:(b + 1) * blk])
+    for h in range(2):
+        o = ref.classification_outputs(q, k, v, geom, h)
+        want = ref.routed_head(q, cache, ref.SPATIAL, h)
+        assert np.array_equal(o.o_spatial, want)
+    big = ref.geometry_of(shape, proxy_mode="cell", cell_h=64, cell_w=64)
+    o = ref.classification_outputs(q, k, v, big, 0)
+    assert np.max(np.abs(o.o_spatial - o.o_full)) < 1e-12
+    # the neighbourhood proxy differs from the cell proxy on this grid
+    o_n = ref.classification_outputs(q, k, v, ref.geometry_of(shape), 0)
+    assert np.max(np.abs(o_n.o_spatial - ref.classification_outputs(q, k, v, geom, 0).o_spatial)) > 1e-3
