@@ -196,13 +196,30 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 #define HC_R32(i) "=r"(r[i])
 #define HC_R32_8(b) HC_R32(b), HC_R32(b + 1), HC_R32(b + 2), HC_R32(b + 3), HC_R32(b + 4), HC_R32(b + 5), \
                     HC_R32(b + 6), HC_R32(b + 7)
-// 32 consecutive TMEM columns of this thread's lane.
+// 32 consecutive TMEM columns of this thread's lane, waited for in the same
+// asm statement so that no use of the registers can be scheduled before the
+// load has completed.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;"
       : HC_R32_8(0), HC_R32_8(8), HC_R32_8(16), HC_R32_8(24)
-      : "r"(taddr));
+      : "r"(taddr)
+      : "memory");
+}
+// Two runs of 32 columns (64 registers) with one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t taddr0, uint32_t taddr1, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : HC_R32_8(0), HC_R32_8(8), HC_R32_8(16), HC_R32_8(24), HC_R32_8(32), HC_R32_8(40), HC_R32_8(48),
+        HC_R32_8(56)
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
 }
 #undef HC_R32
 #define HC_W32(i) "r"(r[i])
@@ -218,7 +235,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
 #undef HC_W32
 #undef HC_R32_8
 #undef HC_W32_8
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -571,7 +587,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t x[32];
         tmem_ld32(t_s + c * 32, x);
-        tmem_wait_ld();
         if (PROXY) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
@@ -604,8 +619,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(t_o + c * 32, o);
-          tmem_wait_ld();
-#pragma unroll
+  #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tmem_st32(t_o + c * 32, o);
         }
@@ -625,9 +639,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         // Keys [64h, 64h+64) of S_i; their probabilities go to P_i columns
         // [32h, 32h+32), which lie inside S_i columns already read.
         uint32_t x[64];
-        tmem_ld32(t_s + h * 64, x);
-        tmem_ld32(t_s + h * 64 + 32, x + 32);
-        tmem_wait_ld();
+        tmem_ld32x2(t_s + h * 64, t_s + h * 64 + 32, x);
         if (PROXY) {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
@@ -665,7 +677,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(t_o + c * 32, o);
-        tmem_wait_ld();
         if (!w) continue;
         if (p.out_fp32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + base + c * 32);
