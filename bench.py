@@ -141,6 +141,19 @@ def path_measurements(hc, shape, cfg, k, v, q, o, flush, stream, reps, peak_tf, 
     return out
 
 
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time: the job's time for weak scaling."""
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank_step, steps, max_ms, world):
+    """Whole-job throughput: the units all ranks processed / the max time."""
+    return world * units_per_rank_step * steps / (max_ms * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi samples taken while the timed region runs."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -738,9 +751,7 @@ def run_ours(args, shape, rank, world, local_rank):
     routed_ms = [r.elapsed_time(b) for _, b, r in evs]
     total_ms = sum(step_ms)
     if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dist, dev)
 
     # In-house full attention on the same queries over the monolithic window,
     # plus the monolithic-ring append it needs (one contiguous copy per block).
@@ -806,7 +817,7 @@ def run_ours(args, shape, rank, world, local_rank):
     mean_routed = statistics.mean(routed_ms)
     achieved = flops / (mean_routed * 1e-3) / 1e12
     tb = traffic_from_profile(f"routed_attention_{shape.name}")
-    value = world * shape.n_q * args.steps / (total_ms * 1e-3)
+    value = job_value(shape.n_q, args.steps, total_ms, world)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,

@@ -42,7 +42,7 @@ EXPORTS = ("hc_abi_version", "hc_status_string", "hc_last_error_message", "hc_co
            "hc_config_validate", "hc_classify_scratch_bytes", "hc_classify", "hc_cache_bytes",
            "hc_cache_create", "hc_cache_destroy", "hc_cache_get_info", "hc_cache_restructure",
            "hc_cache_append", "hc_routed_attention", "hc_full_attention", "hc_get_last_error",
-           "hc_classify_static_scratch")
+           "hc_classify_static_scratch", "hc_debug_inject_stall")
 
 
 class HeadcastUnavailable(RuntimeError):
@@ -112,6 +112,7 @@ def load(path: str = LIB_PATH):
         "hc_full_attention": (C.c_int, [cfgp, vp, vp, vp, i32, i32, vp, vp]),
         "hc_get_last_error": (C.c_int, [vp]),
         "hc_classify_static_scratch": (C.c_int, [cfgp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
+        "hc_debug_inject_stall": (C.c_int, [i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -344,6 +345,13 @@ def hc_full_attention(cfg, q, k, v, o=None, n_key_frames=None, stream=None):
                                     _ptr(v, cfg, "v", (nkf * cfg.F, H, d)), nq, nkf,
                                     _ptr(o, cfg, "o", (nq, H, d)), _stream(stream)))
     return o
+
+
+def hc_debug_inject_stall(enable: bool):
+    """Test hook: while enabled, tensor-core attention launches stall their
+    K/V producer after one tile so that the bounded device waits expire and
+    hc_get_last_error reports HC_ERR_TIMEOUT (outputs undefined)."""
+    _check(load().hc_debug_inject_stall(1 if enable else 0))
 
 
 def hc_get_last_error(stream=None):

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/headcast.h: argument checks,
 // the restructured cache's layout and work list, and kernel launches.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -205,6 +206,9 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
 }
 
 }  // namespace
+
+static std::atomic<int> g_debug_stall{0};
+bool hc::debug_stall_enabled() { return g_debug_stall.load() != 0; }
 
 hc_status hc::record_error(hc_status s, const char* fmt, ...) {
   char buf[512];
@@ -599,6 +603,11 @@ hc_status hc_full_attention(const hc_config* cfg, const void* q, const void* k, 
   } else {
     HC_CUDA(hc::launch_attention(p, cfg->dtype, grid, static_cast<cudaStream_t>(stream)), "full attention");
   }
+  return HC_OK;
+}
+
+hc_status hc_debug_inject_stall(int32_t enable) {
+  g_debug_stall.store(enable != 0 ? 1 : 0);
   return HC_OK;
 }
 

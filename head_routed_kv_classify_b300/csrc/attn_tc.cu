@@ -61,6 +61,7 @@ constexpr int W_PRODUCER = 8, W_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.f;  // rescale O when the row max grows by > 2^8
 constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;   // 1 s
+constexpr unsigned long long STALL_WAIT_LIMIT_NS = 2000000ull; // 2 ms under the stall test hook
 constexpr unsigned long long DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s
 
 template <int D>
@@ -355,6 +356,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
 
   const AttnParams& p = args.p;
   const Geom& g = p.g;
+  const unsigned long long wait_limit = p.wait_limit_ns;
   // Once any CTA has recorded an expired wait, the rest of the launch (and
   // later launches, until the status word is read and cleared) skip their
   // work so that a broken pipeline fails fast.
@@ -420,7 +422,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     if (lane == 0 && n_tiles > 0) {
       const int ycoord = args.kv_head_coord ? it.head : 0;
       int issued_k = 0, issued_v = 0;
+      bool stalled = false;
       for (int t = 0; t < n_tiles; ++t) {
+        if (p.debug_stall && t >= 1) {
+          // Test hook: stop feeding without raising the abort flag, so that
+          // the consumers' bounded waits expire.
+          stalled = true;
+          break;
+        }
         const int st = t % STAGES;
         const uint32_t wpar = ((t / STAGES) - 1) & 1;
         int row;
@@ -430,21 +439,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         } else {
           row = (int)(it.k_row0 + (int64_t)t * BN);
         }
-        if (t >= STAGES && !mbar_wait_bounded(bar(B_KEMPTY + st), wpar, abort_flag, WAIT_LIMIT_NS)) break;
+        if (t >= STAGES && !mbar_wait_bounded(bar(B_KEMPTY + st), wpar, abort_flag, wait_limit)) break;
         mbar_expect_tx(bar(B_KFULL + st), L::KV_BYTES);
 #pragma unroll
         for (int rgn = 0; rgn < L::NREG; ++rgn)
           tma_load_3d(sK + st * L::KV_BYTES + rgn * L::KV_REG, &args.tk, rgn * 64, ycoord, row, bar(B_KFULL + st));
         issued_k = t + 1;
-        if (t >= STAGES && !mbar_wait_bounded(bar(B_VEMPTY + st), wpar, abort_flag, WAIT_LIMIT_NS)) break;
+        if (t >= STAGES && !mbar_wait_bounded(bar(B_VEMPTY + st), wpar, abort_flag, wait_limit)) break;
         mbar_expect_tx(bar(B_VFULL + st), L::KV_BYTES);
 #pragma unroll
         for (int rgn = 0; rgn < L::NREG; ++rgn)
           tma_load_3d(sV + st * L::KV_BYTES + rgn * L::KV_REG, &args.tv, rgn * 64, ycoord, row, bar(B_VFULL + st));
         issued_v = t + 1;
       }
-      if (*abort_flag || issued_v < n_tiles) {
-        *abort_flag = 1;
+      if (stalled || *abort_flag || issued_v < n_tiles) {
+        if (!stalled) *abort_flag = 1;
         // Let the copies still in flight land before the CTA's memory goes.
         volatile int zero_flag = 0;   // drains ignore the abort flag
         for (int t = max(0, issued_k - STAGES); t < issued_k; ++t)
@@ -466,7 +475,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       const uint64_t dk0 = sdesc(sK, 16, 1024);
       const uint64_t dv0 = sdesc(sV, L::KV_REG, 1024);
       auto wait1 = [&](int slot, uint32_t parity) {
-        return mbar_wait_bounded(bar(slot), parity, abort_flag, WAIT_LIMIT_NS);
+        return mbar_wait_bounded(bar(slot), parity, abort_flag, wait_limit);
       };
       // S_i(t) = Q_i K(t)^T into S_i's TMEM columns.
       auto mma_s = [&](int i, int t) {
@@ -551,7 +560,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       proxy_window(g, hq, pos - hq * g.Fw, h_lo, h_hi, w_lo, w_hi);
     }
     auto wait_warp = [&](int slot, uint32_t parity) -> bool {
-      const bool w = mbar_wait_bounded(bar(slot), parity, abort_flag, WAIT_LIMIT_NS);
+      const bool w = mbar_wait_bounded(bar(slot), parity, abort_flag, wait_limit);
       return __all_sync(0xffffffffu, w);
     };
     for (int j = 0; active && j < n_tiles; ++j) {
@@ -780,6 +789,8 @@ cudaError_t launch_attention_tc(const AttnParams& p, const TcKV& kv, dim3 grid, 
   if (e != cudaSuccess) return e;
   if ((e = make_map(&a.tv, kv.v, p.g.d, kv.heads, kv.rows)) != cudaSuccess) return e;
   a.p = p;
+  a.p.debug_stall = debug_stall_enabled() ? 1 : 0;
+  a.p.wait_limit_ns = a.p.debug_stall ? STALL_WAIT_LIMIT_NS : WAIT_LIMIT_NS;
   a.kv_head_coord = kv.heads > 1 ? 1 : 0;
   if (p.item_mode == ITEMS_PROXY)
     return p.g.d == 128 ? launch_d<128, true>(a, grid, s) : launch_d<64, true>(a, grid, s);

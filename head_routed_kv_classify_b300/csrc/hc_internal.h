@@ -115,7 +115,13 @@ struct AttnParams {
   int32_t plane_klen[4];
   Geom g;
   int* status;
+  int32_t debug_stall;        // test hook: the K/V producer stops after the first tile
+  int32_t pad2;
+  uint64_t wait_limit_ns;     // bound of every device-side wait
 };
+
+// Test hook state (hc_debug_inject_stall).
+bool debug_stall_enabled();
 
 // Record a failure message for hc_last_error_message and return `s`.
 hc_status record_error(hc_status s, const char* fmt, ...);

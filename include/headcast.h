@@ -254,6 +254,16 @@ hc_status hc_routed_attention(const hc_cache* cache, const void* q, void* o, voi
 hc_status hc_full_attention(const hc_config* cfg, const void* q, const void* k, const void* v,
                             int32_t n_q_tokens, int32_t n_key_frames, void* o, void* stream);
 
+/* Test hook for the failure path (no counterpart in the paper).  While
+ * enabled (enable != 0), every tensor-core attention launch (routed, full
+ * and classification attention) runs with its K/V producer stopping after
+ * the first key tile and every device-side wait limited to 2 ms: the CTAs'
+ * bounded waits expire, each CTA drains its own copies and MMAs, frees its
+ * tensor memory and returns, and the launch leaves HC_ERR_TIMEOUT in the
+ * device status word (read by hc_get_last_error).  Outputs of such launches
+ * are undefined.  Process-wide; off by default; never faults or hangs. */
+hc_status hc_debug_inject_stall(int32_t enable);
+
 /* SYNC on `stream`: waits for it, returns and clears the device status word
  * (HC_OK, HC_ERR_TIMEOUT for an expired bounded wait, HC_ERR_CUDA for a
  * device-side bounds check).  A CUDA error in the wait is HC_ERR_CUDA. */
