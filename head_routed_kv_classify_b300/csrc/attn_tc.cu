@@ -593,22 +593,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
       for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t x[32];
-        tmem_ld32(t_s + c * 32, x);
+      for (int h = 0; h < BN / 64; ++h) {
+        uint32_t x[64];
+        tmem_ld32x2(t_s + h * 64, t_s + h * 64 + 32, x);
         if (PROXY) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (!((mw[c] >> e) & 1u)) x[e] = __float_as_uint(-INFINITY);
+          for (int e = 0; e < 64; ++e)
+            if (!((mw[2 * h + e / 32] >> (e & 31)) & 1u)) x[e] = __float_as_uint(-INFINITY);
         } else if (!full) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e >= valid) x[e] = __float_as_uint(-INFINITY);
+          for (int e = 0; e < 64; ++e)
+            if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          pm[u] = max3f(pm[u], __uint_as_float(x[4 * u]), __uint_as_float(x[4 * u + 1]));
-          pm[u] = max3f(pm[u], __uint_as_float(x[4 * u + 2]), __uint_as_float(x[4 * u + 3]));
+          pm[u] = max3f(pm[u], __uint_as_float(x[8 * u]), __uint_as_float(x[8 * u + 1]));
+          pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 2]), __uint_as_float(x[8 * u + 3]));
+          pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 4]), __uint_as_float(x[8 * u + 5]));
+          pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 6]), __uint_as_float(x[8 * u + 7]));
         }
       }
       pm[0] = max3f(pm[0], pm[1], pm[2]);
