@@ -75,8 +75,9 @@ def workload_config(shape):
             "parallelism": "replicas (one independent layer per GPU)"}
 
 
-def routed_flops(shape, labels):
-    """Algorithmic FLOPs of routed attention: 4*|q|*|keys|*d per (query, head)."""
+def routed_flops(shape, labels, sliding=False):
+    """Algorithmic FLOPs of routed attention: 4*|q|*|keys|*d per (query, head)
+    (Spatial: the query's cell, or with `sliding` its clipped centred window)."""
     F, d, nq = shape.frame_tokens, shape.head_dim, shape.n_q
     total = 0
     for a in labels:
@@ -84,6 +85,9 @@ def routed_flops(shape, labels):
             keys = nq * shape.n_q
         elif a == synth.GLOBAL:
             keys = nq * shape.n_k
+        elif sliding:
+            keys = nq * shape.window_frames * _window_sum(shape.frame_h) * _window_sum(shape.frame_w) // (
+                shape.frame_h * shape.frame_w)
         else:
             keys = 0
             for hz in _cells(shape.frame_h):
@@ -92,6 +96,12 @@ def routed_flops(shape, labels):
                     keys += (shape.frames_per_block * c) * (shape.window_frames * c)
         total += 4 * keys * d
     return total
+
+
+def _window_sum(n, c=10):
+    """Sum over positions x in [0, n) of the clipped length of the window
+    [x - c//2, x - c//2 + c) on an axis of length n."""
+    return sum(min(n, x - c // 2 + c) - max(0, x - c // 2) for x in range(n))
 
 
 def _cells(n, c=10):
@@ -116,9 +126,10 @@ def path_measurements(hc, shape, cfg, k, v, q, o, flush, stream, reps, peak_tf, 
     import torch
     out = {}
     for arch, name in ((synth.SINK, "sink"), (synth.DUMMY, "dummy"), (synth.SPATIAL, "spatial"),
-                       (synth.GLOBAL, "global")):
+                       (synth.GLOBAL, "global"), (synth.SPATIAL, "spatial_sliding")):
         labels = [arch] * shape.n_heads
-        cache = hc.hc_cache_create(cfg, labels, device=q.device)
+        ccfg = hc.config_for(shape, spatial_mode=hc.HC_SPATIAL_SLIDING) if name == "spatial_sliding" else cfg
+        cache = hc.hc_cache_create(ccfg, labels, device=q.device)
         cache.restructure(k, v, 0)
         times = []
         for i in range(reps + 3):
@@ -131,7 +142,8 @@ def path_measurements(hc, shape, cfg, k, v, q, o, flush, stream, reps, peak_tf, 
                 times.append((a, b))
         torch.cuda.synchronize()
         ms = statistics.mean(x.elapsed_time(y) for x, y in times)
-        fl, by = routed_flops(shape, labels), routed_bytes(shape, labels)
+        fl = routed_flops(shape, labels, sliding=name == "spatial_sliding")
+        by = routed_bytes(shape, labels)
         out[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "gbs": by / (ms * 1e-3) / 1e9,
                      "frac_tensor": fl / (ms * 1e-3) / 1e12 / peak_tf,
                      "frac_hbm": by / (ms * 1e-3) / 1e9 / peak_bw,

@@ -30,11 +30,12 @@ SINK, DUMMY, SPATIAL, GLOBAL = 0, 1, 2, 3
 ARCHETYPES = ("sink", "dummy", "spatial", "global")
 HC_BF16, HC_FP32 = 0, 1
 HC_PROXY_NEIGHBOURHOOD, HC_PROXY_CELL = 0, 1
+HC_SPATIAL_CELLS, HC_SPATIAL_SLIDING = 0, 1
 STATUS_NAMES = {0: "HC_OK", 1: "HC_ERR_INVALID_ARG", 2: "HC_ERR_SHAPE", 3: "HC_ERR_DTYPE",
                 4: "HC_ERR_ALIGN", 5: "HC_ERR_STATE", 6: "HC_ERR_CUDA", 7: "HC_ERR_TIMEOUT",
                 8: "HC_ERR_UNSUPPORTED", 9: "HC_ERR_SIZE"}
 MAX_HEADS = 64
-ABI_VERSION = 2                   # HC_ABI_VERSION this binding is written against
+ABI_VERSION = 3                   # HC_ABI_VERSION this binding is written against
 STATIC_SCRATCH_BYTES = 16 << 20   # HC_STATIC_SCRATCH_BYTES
 
 # Every symbol include/headcast.h declares.
@@ -63,7 +64,7 @@ class HcConfig(C.Structure):
                 ("theta_sink", C.c_float), ("theta_dummy", C.c_float),
                 ("theta_spatial", C.c_float), ("theta_score", C.c_float), ("gamma", C.c_float),
                 ("proxy_radius", C.c_int32), ("cell_h", C.c_int32), ("cell_w", C.c_int32),
-                ("proxy_mode", C.c_int32)]
+                ("proxy_mode", C.c_int32), ("spatial_mode", C.c_int32)]
 
     @property
     def F(self):

@@ -29,6 +29,7 @@ struct hc_cache {
   char* buf;
   size_t bytes, used, off_items, off_k, off_v;
   int n_items;
+  int n_band;            // trailing band items (sliding Spatial heads), launched separately
   int64_t rows;
   int64_t rows_by_arch[4];
   int n_by_arch[4];
@@ -81,6 +82,7 @@ Geom make_geom(const hc_config& c) {
   g.ncell_w = hc::n_cells(c.frame_w, c.cell_w);
   g.radius = c.proxy_radius;
   g.proxy_mode = c.proxy_mode;
+  g.spatial_mode = c.spatial_mode;
   const double scale = c.softmax_scale > 0.f ? (double)c.softmax_scale : 1.0 / std::sqrt((double)c.head_dim);
   g.scale_log2 = (float)(scale * 1.4426950408889634);
   return g;
@@ -116,6 +118,7 @@ int64_t head_rows(const Geom& g, int arch) {
 
 struct Plan {
   std::vector<WorkItem> items;
+  int n_band = 0;
   HeadSlot heads[HC_MAX_HEADS];
   int64_t rows = 0;
   int64_t rows_by_arch[4] = {0, 0, 0, 0};
@@ -165,6 +168,12 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
     } else if (a == HC_GLOBAL) {
       for (int q0 = 0; q0 < g.blk; q0 += BM)
         push(hc::ITEM_RANGE, q0, std::min(BM, g.blk - q0), P.heads[h].row0, 0, g.F, 0);
+    } else if (g.spatial_mode == HC_SPATIAL_SLIDING) {
+      // Runs of up to BM tokens inside one frame of the block; the kernel
+      // derives the band of window rows and masks each query's window.
+      for (int f = 0; f < g.fpb; ++f)
+        for (int t0 = 0; t0 < g.F; t0 += BM)
+          push(hc::ITEM_BAND, f * g.F + t0, std::min(BM, g.F - t0), P.heads[h].row0, 0, g.F, 0);
     } else {
       for (int ci = 0; ci < g.ncell_h; ++ci)
         for (int cj = 0; cj < g.ncell_w; ++cj) {
@@ -189,15 +198,23 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
   auto group = [&](const WorkItem& w) -> int64_t {
     return (int64_t)w.head * (1 << 20) + (w.kind == hc::ITEM_CELL ? w.cell + 1 : 0);
   };
+  // Band items go last, as their own launch of the masked kernel variant.
+  std::stable_partition(P.items.begin(), P.items.end(),
+                        [](const WorkItem& w) { return w.kind != hc::ITEM_BAND; });
+  const auto band0 = std::find_if(P.items.begin(), P.items.end(),
+                                  [](const WorkItem& w) { return w.kind == hc::ITEM_BAND; });
+  P.n_band = (int)(P.items.end() - band0);
   std::map<int64_t, int64_t> group_cost;
   for (const WorkItem& w : P.items) group_cost[group(w)] += cost(w);
-  std::stable_sort(P.items.begin(), P.items.end(), [&](const WorkItem& x, const WorkItem& y) {
+  auto order = [&](const WorkItem& x, const WorkItem& y) {
     const int64_t gx = group(x), gy = group(y);
     const int64_t cx = group_cost[gx], cy = group_cost[gy];
     if (cx != cy) return cx > cy;
     if (gx != gy) return gx < gy;
     return cost(x) > cost(y);
-  });
+  };
+  std::stable_sort(P.items.begin(), band0, order);
+  std::stable_sort(band0, P.items.end(), order);
   const size_t row_bytes = (size_t)g.d * esize_of(cfg.dtype);
   P.off_items = 256;
   P.off_k = round_up(P.off_items + P.items.size() * sizeof(WorkItem), 256);
@@ -289,6 +306,8 @@ hc_status hc_config_validate(const hc_config* c) {
     return fail(HC_ERR_INVALID_ARG, "proxy_radius %d / cell %dx%d", c->proxy_radius, c->cell_h, c->cell_w);
   if (c->proxy_mode != HC_PROXY_NEIGHBOURHOOD && c->proxy_mode != HC_PROXY_CELL)
     return fail(HC_ERR_INVALID_ARG, "proxy_mode %d is not 0 or 1", c->proxy_mode);
+  if (c->spatial_mode != HC_SPATIAL_CELLS && c->spatial_mode != HC_SPATIAL_SLIDING)
+    return fail(HC_ERR_INVALID_ARG, "spatial_mode %d is not 0 or 1", c->spatial_mode);
   return HC_OK;
 }
 
@@ -442,6 +461,7 @@ hc_status hc_cache_create(const hc_config* cfg, const int8_t* labels_host, void*
   c->off_k = P.off_k;
   c->off_v = P.off_v;
   c->n_items = (int)P.items.size();
+  c->n_band = P.n_band;
   c->rows = P.rows;
   for (int a = 0; a < 4; ++a) {
     c->rows_by_arch[a] = P.rows_by_arch[a];
@@ -557,9 +577,20 @@ hc_status hc_routed_attention(const hc_cache* c, const void* q, void* o, void* s
   p.status = status;
   if (c->cfg.dtype == HC_BF16) {
     const hc::TcKV kv{c->buf + c->off_k, c->buf + c->off_v, 1, c->rows};
-    HC_CUDA(hc::launch_attention_tc(p, kv, dim3(c->n_items, 1, 1), static_cast<cudaStream_t>(stream)),
-            "routed attention");
+    const int n_main = c->n_items - c->n_band;
+    if (n_main > 0)
+      HC_CUDA(hc::launch_attention_tc(p, kv, dim3(n_main, 1, 1), static_cast<cudaStream_t>(stream)),
+              "routed attention");
+    if (c->n_band > 0) {
+      // Sliding Spatial heads: the masked band variant over the list's tail.
+      p.items += n_main;
+      p.n_items = c->n_band;
+      p.band_win = hc::WIN_SLIDING;
+      HC_CUDA(hc::launch_attention_tc(p, kv, dim3(c->n_band, 1, 1), static_cast<cudaStream_t>(stream)),
+              "routed attention (sliding Spatial)");
+    }
   } else {
+    p.band_win = hc::WIN_SLIDING;
     HC_CUDA(hc::launch_attention(p, c->cfg.dtype, dim3(c->n_items, 1, 1), static_cast<cudaStream_t>(stream)),
             "routed attention");
   }

@@ -54,6 +54,16 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p) {
       it.hz = cell_extent(ci, g.Fh, g.cell_h, g.ncell_h);
       it.w0 = cj * g.cell_w;
       it.wz = cell_extent(cj, g.Fw, g.cell_w, g.ncell_w);
+    } else if (w.kind == ITEM_BAND) {
+      // Sliding Spatial: band of window rows over the head's filled ring slots.
+      const int t0 = w.q0 % g.F;
+      int hmin = t0 / g.Fw, hmax = (t0 + it.nq - 1) / g.Fw;
+      int lo, hi, wl, wh, rhi;
+      band_window(g, p.band_win, hmin, 0, it.rlo, hi, wl, wh);
+      band_window(g, p.band_win, hmax, 0, lo, rhi, wl, wh);
+      it.range_len = (rhi - it.rlo + 1) * g.Fw;
+      it.tpr = (it.range_len + BN - 1) / BN;
+      it.k_len = p.valid_frames * it.range_len;
     }
   } else if (p.item_mode == ITEMS_DENSE) {
     it.head = blockIdx.y;
@@ -74,14 +84,16 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p) {
     int hmin = (t * kBM) / g.Fw;
     int hmax = (t * kBM + it.nq - 1) / g.Fw;
     int lo, hi, wl, wh, rhi;
-    proxy_window(g, hmin, 0, it.rlo, hi, wl, wh);
-    proxy_window(g, hmax, 0, lo, rhi, wl, wh);
+    band_window(g, WIN_PROXY, hmin, 0, it.rlo, hi, wl, wh);
+    band_window(g, WIN_PROXY, hmax, 0, lo, rhi, wl, wh);
     it.range_len = (rhi - it.rlo + 1) * g.Fw;
     it.tpr = (it.range_len + BN - 1) / BN;
     it.k_len = p.proxy_frames * it.range_len;
   }
   if (it.kind == ITEM_PROXY)
     it.n_tiles = p.proxy_frames * it.tpr;
+  else if (it.kind == ITEM_BAND)
+    it.n_tiles = p.valid_frames * it.tpr;
   else
     it.n_tiles = it.k_len > 0 ? (it.k_len + BN - 1) / BN : 0;
   return it;
@@ -102,10 +114,10 @@ __device__ __forceinline__ int query_token(const Item& it, const Geom& g, int r)
 template <int BN>
 __device__ __forceinline__ void tile_rows(const Item& it, const Geom& g, int t, int64_t& row,
                                           int& valid, int& pos0) {
-  if (it.kind == ITEM_PROXY) {
+  if (it.kind == ITEM_PROXY || it.kind == ITEM_BAND) {
     int f = t / it.tpr, o = (t - f * it.tpr) * BN;
     pos0 = it.rlo * g.Fw + o;
-    row = (int64_t)f * g.F + pos0;
+    row = it.k_row0 + (int64_t)f * g.F + pos0;
     valid = min(BN, it.range_len - o);
   } else {
     row = it.k_row0 + (int64_t)t * BN;
@@ -137,10 +149,12 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnParams p) {
     for (int c = lane; c < D; c += 32) sq[warp][c] = Q[tok * HD + it.head * D + c];
     __syncwarp();
     int h_lo = 0, h_hi = 0, w_lo = 0, w_hi = 0;
-    if (it.kind == ITEM_PROXY) {
+    const bool band = it.kind == ITEM_PROXY || it.kind == ITEM_BAND;
+    if (band) {
       const int tp = tok % g.F;
       const int hq = tp / g.Fw;
-      proxy_window(g, hq, tp - hq * g.Fw, h_lo, h_hi, w_lo, w_hi);
+      band_window(g, it.kind == ITEM_BAND ? p.band_win : (int)WIN_PROXY, hq, tp - hq * g.Fw, h_lo, h_hi, w_lo,
+                  w_hi);
     }
     float m = -CUDART_INF_F, l = 0.f, acc[PER];
 #pragma unroll
@@ -150,7 +164,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnParams p) {
       int valid, pos0;
       tile_rows<BN>(it, g, t, row0, valid, pos0);
       bool ok = lane < valid;
-      if (ok && it.kind == ITEM_PROXY) {
+      if (ok && band) {
         int pos = pos0 + lane;
         int hk = pos / g.Fw, wk = pos - hk * g.Fw;
         ok = hk >= h_lo && hk <= h_hi && wk >= w_lo && wk <= w_hi;

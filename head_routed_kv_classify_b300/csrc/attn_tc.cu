@@ -28,9 +28,11 @@
 // execute in order.  The commit that signals S_i(j) also covers
 // P_i(j-1) V(j-1), so a softmax group may rescale O_i as soon as it sees
 // S_i(j).
-// The classification proxy (ITEMS_PROXY) runs the same pipeline on the band
-// of frame rows around a run of query tokens in every window frame, with a
-// per-row (2r+1) x (2r+1) neighbourhood mask applied to S before the softmax.
+// Band items -- the classification proxy (ITEMS_PROXY) and, with sliding
+// deployed Spatial heads, their routed items (ITEM_BAND) -- run the same
+// pipeline on the band of frame rows around a run of query tokens in every
+// frame, with a per-row window mask (the (2r+1) x (2r+1) neighbourhood, the
+// deployed cell, or the centred cell_h x cell_w window) applied to S.
 // Hand-offs are mbarriers; every wait is bounded in wall-clock time and on
 // expiry the CTA records HC_ERR_TIMEOUT in the status word, drains its own
 // copies and MMAs (again bounded), frees TMEM and returns.
@@ -275,8 +277,20 @@ struct TcItem {
   int64_t k_row0;
   int k_len;
   int h0, w0, hz, wz;   // ITEM_CELL: the cell
-  int rlo, rlen, tpf;   // ITEM_PROXY: first band row, keys per frame band, key tiles per frame
+  int rlo, rlen, tpf;   // band items: first band row, keys per frame band, key tiles per frame
 };
+
+// Band of frame rows [h_lo(first row), h_hi(last row)] of a run of queries
+// [t0, t0 + nq) inside one frame, over `frames` frames of keys.
+__device__ __forceinline__ void tc_band(TcItem& it, const Geom& g, int win, int t0, int frames) {
+  const int hmin = t0 / g.Fw, hmax = (t0 + it.nq - 1) / g.Fw;
+  int lo, rhi, wl, wh;
+  band_window(g, win, hmin, 0, it.rlo, rhi, wl, wh);
+  band_window(g, win, hmax, 0, lo, rhi, wl, wh);
+  it.rlen = (rhi - it.rlo + 1) * g.Fw;
+  it.tpf = (it.rlen + BN - 1) / BN;
+  it.k_len = frames * it.tpf * BN;
+}
 
 __device__ __forceinline__ TcItem tc_decode(const AttnParams& p) {
   const Geom& g = p.g;
@@ -294,13 +308,7 @@ __device__ __forceinline__ TcItem tc_decode(const AttnParams& p) {
     it.nq = min(QT * BM, g.F - t0);
     it.out_plane = 3;
     it.k_row0 = 0;
-    const int hmin = t0 / g.Fw, hmax = (t0 + it.nq - 1) / g.Fw;
-    int lo, rhi, wl, wh;
-    proxy_window(g, hmin, 0, it.rlo, rhi, wl, wh);
-    proxy_window(g, hmax, 0, lo, rhi, wl, wh);
-    it.rlen = (rhi - it.rlo + 1) * g.Fw;
-    it.tpf = (it.rlen + BN - 1) / BN;
-    it.k_len = p.proxy_frames * it.tpf * BN;
+    tc_band(it, g, WIN_PROXY, t0, p.proxy_frames);
   } else if (p.item_mode == ITEMS_LIST) {
     const WorkItem w = p.items[blockIdx.x];
     it.head = w.head;
@@ -316,6 +324,9 @@ __device__ __forceinline__ TcItem tc_decode(const AttnParams& p) {
       it.hz = cell_extent(ci, g.Fh, g.cell_h, g.ncell_h);
       it.w0 = cj * g.cell_w;
       it.wz = cell_extent(cj, g.Fw, g.cell_w, g.ncell_w);
+    } else if (w.kind == ITEM_BAND) {
+      // Sliding Spatial: the head's ring slots in raster order from k_row0.
+      tc_band(it, g, p.band_win, w.q0 % g.F, p.valid_frames);
     }
   } else {  // ITEMS_DENSE
     it.head = blockIdx.y;
@@ -435,7 +446,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         int row;
         if (PROXY) {
           const int f = t / it.tpf;
-          row = f * g.F + it.rlo * g.Fw + (t - f * it.tpf) * BN;
+          row = (int)it.k_row0 + f * g.F + it.rlo * g.Fw + (t - f * it.tpf) * BN;
         } else {
           row = (int)(it.k_row0 + (int64_t)t * BN);
         }
@@ -557,7 +568,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     if (PROXY) {
       const int pos = (it.q0 + qrow) % g.F;
       const int hq = pos / g.Fw;
-      proxy_window(g, hq, pos - hq * g.Fw, h_lo, h_hi, w_lo, w_hi);
+      band_window(g, p.band_win, hq, pos - hq * g.Fw, h_lo, h_hi, w_lo, w_hi);
     }
     auto wait_warp = [&](int slot, uint32_t parity) -> bool {
       const bool w = mbar_wait_bounded(bar(slot), parity, abort_flag, wait_limit);
@@ -794,7 +805,9 @@ cudaError_t launch_attention_tc(const AttnParams& p, const TcKV& kv, dim3 grid, 
   a.p.debug_stall = debug_stall_enabled() ? 1 : 0;
   a.p.wait_limit_ns = a.p.debug_stall ? STALL_WAIT_LIMIT_NS : WAIT_LIMIT_NS;
   a.kv_head_coord = kv.heads > 1 ? 1 : 0;
-  if (p.item_mode == ITEMS_PROXY)
+  // Band items (classification proxy, routed sliding Spatial) run the masked
+  // variant; the caller launches them separately from the other items.
+  if (p.item_mode == ITEMS_PROXY || p.band_win == WIN_SLIDING)
     return p.g.d == 128 ? launch_d<128, true>(a, grid, s) : launch_d<64, true>(a, grid, s);
   return p.g.d == 128 ? launch_d<128, false>(a, grid, s) : launch_d<64, false>(a, grid, s);
 }

@@ -7,6 +7,7 @@
 //   Sink     block 0 only, rows [0, 3F)
 //   Dummy    the newest block only, rows [0, 3F)
 //   Global   ring slot s = a mod W, rows [s*F, (s+1)*F) in raster order
+//            (also Spatial heads in the sliding mode)
 //   Spatial  ring slot s, cell-major: cell (ci, cj) owns rows
 //            W*tokens_before(ci, cj) + [0, W*|cell|), slot s of it the
 //            |cell| rows at offset s*|cell|, row-major inside the cell
@@ -43,7 +44,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const ScatterParams p) {
     } else if (hs.arch == HC_DUMMY) {
       if (a < p.dummy_frame0) continue;
       row = (a - p.dummy_frame0) * g.F + pos;
-    } else if (hs.arch == HC_GLOBAL) {
+    } else if (hs.arch == HC_GLOBAL || g.spatial_mode == HC_SPATIAL_SLIDING) {
       row = (a % g.Wf) * g.F + pos;
     } else {
       const int slot = (int)(a % g.Wf);

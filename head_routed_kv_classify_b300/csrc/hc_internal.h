@@ -23,6 +23,7 @@ struct Geom {
   int cell_h, cell_w, ncell_h, ncell_w;
   int radius;
   int proxy_mode;                      // HC_PROXY_NEIGHBOURHOOD or HC_PROXY_CELL
+  int spatial_mode;                    // HC_SPATIAL_CELLS or HC_SPATIAL_SLIDING
   float scale_log2;                    // softmax scale * log2(e)
 };
 
@@ -66,11 +67,33 @@ HC_HD void proxy_window(const Geom& g, int h, int w, int& h_lo, int& h_hi, int& 
   }
 }
 
+// Rows and columns of the sliding deployed Spatial window of a query at
+// (h, w): cell_h x cell_w keys with the query at offset (cell_h/2, cell_w/2)
+// from the top-left corner, clipped.  Bounds non-decreasing in h and w.
+HC_HD void sliding_window(const Geom& g, int h, int w, int& h_lo, int& h_hi, int& w_lo, int& w_hi) {
+  const int h0 = h - g.cell_h / 2, w0 = w - g.cell_w / 2;
+  h_lo = h0 < 0 ? 0 : h0;
+  h_hi = h0 + g.cell_h - 1 > g.Fh - 1 ? g.Fh - 1 : h0 + g.cell_h - 1;
+  w_lo = w0 < 0 ? 0 : w0;
+  w_hi = w0 + g.cell_w - 1 > g.Fw - 1 ? g.Fw - 1 : w0 + g.cell_w - 1;
+}
+
+// Window of a band item: the classification proxy or the sliding Spatial path.
+enum : int32_t { WIN_PROXY = 0, WIN_SLIDING = 1 };
+HC_HD void band_window(const Geom& g, int win, int h, int w, int& h_lo, int& h_hi, int& w_lo, int& w_hi) {
+  if (win == WIN_SLIDING)
+    sliding_window(g, h, w, h_lo, h_hi, w_lo, w_hi);
+  else
+    proxy_window(g, h, w, h_lo, h_hi, w_lo, w_hi);
+}
+
 // Work item kinds.
 enum : int32_t {
   ITEM_RANGE = 0,   // queries q0.. (block-local tokens), keys: one run of rows
   ITEM_CELL = 1,    // queries: ordinals q0.. of one cell's 3-frame query set
   ITEM_PROXY = 2,   // queries q0.. inside one frame; keys: (2r+1) neighbourhood rows of every frame
+  ITEM_BAND = 3,    // routed sliding Spatial: queries q0.. inside one frame; keys: the band
+                    // of window rows in every filled ring slot of the head, masked per query
 };
 
 struct alignas(16) WorkItem {
@@ -115,8 +138,8 @@ struct AttnParams {
   int32_t plane_klen[4];
   Geom g;
   int* status;
+  int32_t band_win;           // WIN_PROXY / WIN_SLIDING window of band items
   int32_t debug_stall;        // test hook: the K/V producer stops after the first tile
-  int32_t pad2;
   uint64_t wait_limit_ns;     // bound of every device-side wait
 };
 

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define HC_ABI_VERSION 2
+#define HC_ABI_VERSION 3
 #define HC_MAX_HEADS 64
 
 typedef enum { HC_SINK = 0, HC_DUMMY = 1, HC_SPATIAL = 2, HC_GLOBAL = 3 } hc_archetype;
@@ -98,7 +98,16 @@ typedef struct {
                                clipped (2r+1)x(2r+1) neighbourhood of the query;
                                HC_PROXY_CELL (1) = the query's deployed cell
                                (compares the proxy with the deployed path)    */
+  int32_t spatial_mode;     /* deployed Spatial key set:
+                               HC_SPATIAL_CELLS (0, default) = the query's own
+                               non-overlapping cell_h x cell_w cell;
+                               HC_SPATIAL_SLIDING (1) = the cell_h x cell_w
+                               window centred on the query (rows
+                               h - cell_h/2 .. h + cell_h - cell_h/2 - 1,
+                               columns likewise, clipped), in every frame     */
 } hc_config;
+
+typedef enum { HC_SPATIAL_CELLS = 0, HC_SPATIAL_SLIDING = 1 } hc_spatial_mode;
 
 typedef enum { HC_PROXY_NEIGHBOURHOOD = 0, HC_PROXY_CELL = 1 } hc_proxy_mode;
 
@@ -126,7 +135,8 @@ const char* hc_last_error_message(void);
  * frames_per_block = 3, window_frames = 21, dtype = HC_BF16. */
 hc_status hc_config_default(hc_config* out);
 /* Check a config: H in 1..64, d in {64,128}, frame dims >= 1, window a
- * positive multiple of frames_per_block, finite thresholds, proxy_mode 0/1. */
+ * positive multiple of frames_per_block, finite thresholds, proxy_mode and
+ * spatial_mode 0/1. */
 hc_status hc_config_validate(const hc_config* cfg);
 
 /* ---------------------------------------------------------------------------
@@ -201,7 +211,8 @@ hc_status hc_classify_static_scratch(const hc_config* cfg, const void* q, const 
  *   Spatial head  window_frames*F rows: a ring of frame slots (frame a lives
  *                 in slot a mod window_frames), stored cell-major: all slots
  *                 of one cell are contiguous, so a cell's keys across the
- *                 window form one run of rows;
+ *                 window form one run of rows (with HC_SPATIAL_SLIDING, in
+ *                 raster order like a Global head);
  *   Global head   window_frames*F rows: the same ring in raster order.
  * K rows of all heads form one [rows][d] area, V rows a second one.
  * [Pith review, "What carries the argument" (split along the head
@@ -242,8 +253,9 @@ hc_status hc_cache_append(hc_cache* cache, int64_t block_id, const void* k_blk,
  * Routed attention: every head over its own pathway, one launch.
  * q, o  [3F][H][d] the current block's queries / outputs.
  * softmax(q k^T * scale) v over: Sink -> block 0; Dummy -> newest block;
- * Spatial -> the query's cell in every filled ring slot; Global -> every
- * filled ring slot.  No mask inside a block.  Async.
+ * Spatial -> the query's cell in every filled ring slot (HC_SPATIAL_SLIDING:
+ * the window centred on the query); Global -> every filled ring slot.  No
+ * mask inside a block.  Async (one launch; two with sliding Spatial heads).
  * [Pith review, "The pith", "Core claim", Figure 3 caption.]
  * ------------------------------------------------------------------------- */
 hc_status hc_routed_attention(const hc_cache* cache, const void* q, void* o, void* stream);

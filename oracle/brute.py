@@ -44,11 +44,17 @@ def in_cell(qh, qw, kh, kw, frame_h, frame_w, cell_h, cell_w):
             axis_cell(qw, frame_w, cell_w) == axis_cell(kw, frame_w, cell_w))
 
 
+def in_sliding(qh, qw, kh, kw, cell_h, cell_w):
+    """Window of cell_h x cell_w keys with the query at offset (cell_h//2,
+    cell_w//2) from its top-left corner."""
+    return 0 <= kh - qh + cell_h // 2 < cell_h and 0 <= kw - qw + cell_w // 2 < cell_w
+
+
 def keyset_outputs(q, k, v, head, frame_h, frame_w, block_tokens, kind, scale,
                    radius=2, cell_h=10, cell_w=10):
     """Outputs of one head for every query, over the key set ``kind``:
     'full', 'sink' (window's first block), 'dummy' (last block), 'proxy',
-    'cell'.  q, k, v are nested lists or arrays [tokens][H][d]."""
+    'cell', 'sliding'.  q, k, v are nested lists or arrays [tokens][H][d]."""
     nk = len(k)
     out = []
     for i in range(len(q)):
@@ -66,6 +72,8 @@ def keyset_outputs(q, k, v, head, frame_h, frame_w, block_tokens, kind, scale,
                 ok = in_proxy(qh, qw, kh, kw, radius)
             elif kind == "cell":
                 ok = in_cell(qh, qw, kh, kw, frame_h, frame_w, cell_h, cell_w)
+            elif kind == "sliding":
+                ok = in_sliding(qh, qw, kh, kw, cell_h, cell_w)
             else:
                 raise ValueError(kind)
             if ok:

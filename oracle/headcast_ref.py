@@ -76,6 +76,12 @@ class Geometry:
     # paper's (2r+1)x(2r+1) window) or "cell" (the deployed cell, to measure
     # how well the proxy stands for the deployed path) [HC-pith major comment 2].
     proxy_mode: str = "neighbourhood"
+    # Deployed Spatial key set: "cells" (the query's own non-overlapping
+    # cell, the reading of the pages' "non-overlapping 10x10 cells") or
+    # "sliding" (the cell_h x cell_w window centred on the query, rows
+    # h - cell_h//2 .. h + cell_h - cell_h//2 - 1 and likewise for columns,
+    # clipped; the "10x10 grid around the query's position" wording).
+    spatial_mode: str = "cells"
 
     @property
     def F(self):
@@ -193,6 +199,17 @@ def cell_keys(h, w, n_frames, geom: Geometry):
     return np.array([f * geom.F + hh * geom.frame_w + ww
                      for f in range(n_frames)
                      for hh in range(h0, h0 + hz) for ww in range(w0, w0 + wz)], dtype=np.int64)
+
+
+def sliding_keys(h, w, n_frames, geom: Geometry):
+    """Deployed Spatial path, sliding variant: the cell_h x cell_w window
+    whose rows are h - cell_h//2 .. h + cell_h - cell_h//2 - 1 (columns
+    likewise), clipped to the frame, in every window frame."""
+    h0, w0 = h - geom.cell_h // 2, w - geom.cell_w // 2
+    hs = range(max(0, h0), min(geom.frame_h, h0 + geom.cell_h))
+    ws = range(max(0, w0), min(geom.frame_w, w0 + geom.cell_w))
+    return np.array([f * geom.F + hh * geom.frame_w + ww
+                     for f in range(n_frames) for hh in hs for ww in ws], dtype=np.int64)
 
 
 def attend_by_position(q_h, k_h, v_h, geom: Geometry, n_frames, keyset, scale, query_idx):
@@ -383,7 +400,8 @@ def routed_head(q, cache: CacheModel, label, head, scale=None, query_idx=None):
     kh, vh = k[:, head, :], v[:, head, :]
     if label == SPATIAL:
         n_frames = kh.shape[0] // geom.F
-        return attend_by_position(qh, kh, vh, geom, n_frames, cell_keys, scale, qi)
+        keyset = sliding_keys if geom.spatial_mode == "sliding" else cell_keys
+        return attend_by_position(qh, kh, vh, geom, n_frames, keyset, scale, qi)
     return attend_chunked(qh[qi], kh, vh, scale)
 
 

@@ -47,7 +47,7 @@ def test_library_does_not_need_libcuda(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.hc_abi_version() == hc.ABI_VERSION == 2
+    assert lib.hc_abi_version() == hc.ABI_VERSION == 3
     assert lib.hc_status_string(0) == b"ok"
     assert lib.hc_status_string(7) == b"device-side wait expired"
 
@@ -68,6 +68,7 @@ def test_config_default_holds_ledger_constants(lib):
     ("theta_sink", float("nan"), "HC_ERR_INVALID_ARG"), ("softmax_scale", -1.0, "HC_ERR_INVALID_ARG"),
     ("cell_w", 0, "HC_ERR_INVALID_ARG"), ("proxy_radius", -1, "HC_ERR_INVALID_ARG"),
     ("proxy_mode", 2, "HC_ERR_INVALID_ARG"), ("proxy_mode", -1, "HC_ERR_INVALID_ARG"),
+    ("spatial_mode", 2, "HC_ERR_INVALID_ARG"),
 ])
 def test_config_validation(lib, field, value, status):
     cfg = hc.make_config(12, 128, 45, 80)

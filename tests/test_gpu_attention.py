@@ -154,3 +154,46 @@ def test_routed_and_full_sampled_full_size(name):
     want_f = ref.full_attention(inp.q.values, inp.k.values, inp.v.values, query_idx=idx2)
     gu.assert_close(of[idx2], want_f, "bf16", f"{name} full sample")
     hc.hc_get_last_error()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_routed_sliding_spatial_small(name):
+    """The sliding deployed Spatial variant (the cell_h x cell_w window
+    centred on the query): Spatial heads stored in raster order and run as
+    band items of the masked kernel, next to the other pathways."""
+    shape, inp = _inputs(name)
+    cfg = hc.config_for(shape, spatial_mode=hc.HC_SPATIAL_SLIDING)
+    geom = ref.geometry_of(shape, spatial_mode="sliding")
+    cache_ref = ref.CacheModel(geom)
+    blk = shape.n_q
+    for b in range(shape.blocks_per_window):
+        cache_ref.put(b, inp.k.values[b * blk:(b + 1) * blk], inp.v.values[b * blk:(b + 1) * blk])
+    for labels in (np.array(inp.planted, np.int8), np.full(shape.n_heads, 2, np.int8)):
+        cache = hc.hc_cache_create(cfg, labels)
+        cache.restructure(gu.to_dev(inp.k, shape.dtype), gu.to_dev(inp.v, shape.dtype), 0)
+        o = gu.to_host(cache.routed_attention(gu.to_dev(inp.q, shape.dtype)))
+        want = ref.routed_attention(inp.q.values, cache_ref, labels)
+        gu.assert_close(o, want, shape.dtype, f"sliding {name} {list(labels)}")
+        hc.hc_get_last_error()
+
+
+def test_routed_sliding_spatial_720p_sampled_with_append():
+    shape, inp = _inputs("720p")
+    cfg = hc.config_for(shape, spatial_mode=hc.HC_SPATIAL_SLIDING)
+    geom = ref.geometry_of(shape, spatial_mode="sliding")
+    cache_ref = ref.CacheModel(geom)
+    blk = shape.n_q
+    for b in range(shape.blocks_per_window):
+        cache_ref.put(b, inp.k.values[b * blk:(b + 1) * blk], inp.v.values[b * blk:(b + 1) * blk])
+    labels = np.array(inp.planted, np.int8)
+    cache = hc.hc_cache_create(cfg, labels)
+    cache.restructure(gu.to_dev(inp.k, "bf16"), gu.to_dev(inp.v, "bf16"), 0)
+    bq, bk, bv = synth.make_block(shape, seed=404)
+    nb = shape.blocks_per_window
+    cache.append(nb, gu.to_dev(bk, "bf16"), gu.to_dev(bv, "bf16"))
+    cache_ref.put(nb, bk.values, bv.values)
+    o = gu.to_host(cache.routed_attention(gu.to_dev(bq, "bf16")))
+    idx = gu.sample_queries(shape.n_q, 40, seed=77)
+    want = ref.routed_attention(bq.values, cache_ref, labels, query_idx=idx)
+    gu.assert_close(o[idx], want, "bf16", "720p sliding sample")
+    hc.hc_get_last_error()

@@ -7,6 +7,7 @@ brute-force twin that decides key membership by predicate, and invariants of
 the key sets.  A dropped term, a wrong sign or index, or a transposed operand
 in the oracle fails at least one of them.
 """
+import dataclasses
 import json
 import math
 import os
@@ -102,9 +103,11 @@ def test_block_sets_equal_masked_full_attention():
             assert np.allclose(got, p @ v[:, h, :], atol=1e-12)
 
 
-@pytest.mark.parametrize("kind", ["full", "sink", "dummy", "proxy", "cell"])
+@pytest.mark.parametrize("kind", ["full", "sink", "dummy", "proxy", "cell", "sliding"])
 def test_brute_force_twin(kind):
     geom = tiny_geom()
+    if kind == "sliding":
+        geom = dataclasses.replace(geom, spatial_mode="sliding", cell_h=4, cell_w=3)
     q, k, v = rand_qkv(geom, 4)
     scale = 1 / math.sqrt(geom.head_dim)
     for h in range(geom.n_heads):
@@ -112,7 +115,7 @@ def test_brute_force_twin(kind):
                                              geom.block_tokens, kind, scale,
                                              radius=geom.proxy_radius, cell_h=geom.cell_h,
                                              cell_w=geom.cell_w))
-        if kind == "cell":
+        if kind in ("cell", "sliding"):
             cache = ref.CacheModel(geom)
             for b in range(geom.blocks_per_window):
                 sl = slice(b * geom.block_tokens, (b + 1) * geom.block_tokens)
@@ -355,3 +358,28 @@ def test_cell_proxy_mode_uses_the_deployed_cells():
     # the neighbourhood proxy differs from the cell proxy on this grid
     o_n = ref.classification_outputs(q, k, v, ref.geometry_of(shape), 0)
     assert np.max(np.abs(o_n.o_spatial - ref.classification_outputs(q, k, v, geom, 0).o_spatial)) > 1e-3
+
+
+def test_sliding_window_pins():
+    """The sliding Spatial key set: a centred window covering the grid from
+    every position equals Global; an interior query of a 10x10 window sees
+    exactly 100 keys per frame with itself at offset (5, 5); at a corner the
+    window is clipped to rows/cols 0..4."""
+    geom = tiny_geom()
+    big = dataclasses.replace(geom, spatial_mode="sliding", cell_h=2 * geom.frame_h, cell_w=2 * geom.frame_w)
+    q, k, v = rand_qkv(geom, 5)
+    cache = ref.CacheModel(big)
+    for b in range(geom.blocks_per_window):
+        sl = slice(b * geom.block_tokens, (b + 1) * geom.block_tokens)
+        cache.put(b, k[sl], v[sl])
+    for h in range(geom.n_heads):
+        got = ref.routed_head(q, cache, ref.SPATIAL, h)
+        want = ref.full_attention(q, k, v)[:, h, :]
+        assert np.max(np.abs(got - want)) < 1e-12
+    g = ref.Geometry(1, 8, 30, 52, 21, spatial_mode="sliding")
+    keys = ref.sliding_keys(12, 20, 1, g)
+    assert len(keys) == 100
+    rows, cols = keys // 52, keys % 52
+    assert rows.min() == 7 and rows.max() == 16 and cols.min() == 15 and cols.max() == 24
+    corner = ref.sliding_keys(0, 0, 2, g)
+    assert len(corner) == 2 * 25 and (corner % g.F // 52).max() == 4 and (corner % g.F % 52).max() == 4
