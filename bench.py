@@ -256,17 +256,50 @@ def traffic_from_profile(kernel_tag):
 
 # --------------------------------------------------------------------------- oracle arms
 
-def oracle_step_sample(shape, inp, labels, n_queries, seed):
-    from oracle import headcast_ref as ref
-    geom = ref.geometry_of(shape)
-    cache = ref.CacheModel(geom)
-    blk = shape.n_q
-    for b in range(shape.blocks_per_window):
-        cache.put(b, inp.k.values[b * blk:(b + 1) * blk], inp.v.values[b * blk:(b + 1) * blk])
-    idx = np.sort(np.random.default_rng(seed).choice(shape.n_q, n_queries, replace=False))
-    t0 = time.perf_counter()
-    ref.routed_attention(inp.q.values, cache, labels, query_idx=idx)
-    return time.perf_counter() - t0
+class OracleStep:
+    """The oracle's routed attention for a query sample of one layer.
+
+    Set-up (untimed) puts the window's blocks in the oracle's cache model and
+    takes each head's pathway keys and values out of it once (the oracle's
+    routed_attention rebuilds the whole window for every head on every call,
+    several seconds at 720P that would swamp a small sample); a timed step
+    then runs the oracle's own attention routines on the sample: the dense
+    softmax attention for Sink, Dummy and Global heads and the per-position
+    cell attention for Spatial heads."""
+
+    def __init__(self, shape, inp, labels):
+        from oracle import headcast_ref as ref
+        self.ref = ref
+        self.geom = ref.geometry_of(shape)
+        cache = ref.CacheModel(self.geom)
+        blk = shape.n_q
+        for b in range(shape.blocks_per_window):
+            cache.put(b, inp.k.values[b * blk:(b + 1) * blk], inp.v.values[b * blk:(b + 1) * blk])
+        win_k, win_v = cache.window()
+        sink_k, sink_v = cache.sink()
+        cur_k, cur_v = cache.current()
+        self.q = inp.q.values
+        self.scale = ref.default_scale(shape.head_dim)
+        self.labels = [int(a) for a in labels]
+        self.kv = []
+        for h, a in enumerate(self.labels):
+            k, v = {ref.SINK: (sink_k, sink_v), ref.DUMMY: (cur_k, cur_v)}.get(a, (win_k, win_v))
+            self.kv.append((np.ascontiguousarray(k[:, h, :]), np.ascontiguousarray(v[:, h, :])))
+        self.n_q = shape.n_q
+
+    def __call__(self, n_queries, seed):
+        ref = self.ref
+        idx = np.sort(np.random.default_rng(seed).choice(self.n_q, n_queries, replace=False))
+        t0 = time.perf_counter()
+        for h, a in enumerate(self.labels):
+            qh = np.asarray(self.q[:, h, :], np.float64)
+            kh, vh = self.kv[h]
+            if a == ref.SPATIAL:
+                ref.attend_by_position(qh, kh, vh, self.geom, kh.shape[0] // self.geom.F, ref.cell_keys,
+                                       self.scale, idx)
+            else:
+                ref.attend_chunked(qh[idx], kh, vh, self.scale)
+        return time.perf_counter() - t0
 
 
 def blas_threads():
@@ -280,10 +313,11 @@ def blas_threads():
 
 def cpu_baseline(shape, inp, labels, seconds):
     """The oracle as it stands, on growing query samples until ~seconds of work."""
+    step = OracleStep(shape, inp, labels)
     done, spent, n = 0, 0.0, 16
     seed = 0
     while spent < seconds:
-        spent += oracle_step_sample(shape, inp, labels, n, seed)
+        spent += step(n, seed)
         done += n
         seed += 1
         n = min(2 * n, 256)
@@ -292,24 +326,30 @@ def cpu_baseline(shape, inp, labels, seconds):
                       f"{shape.name} layer, fp64 NumPy, {spent:.1f} s"}
 
 
-def run_reference(args, shape, rank, world):
+def run_reference(args, shape, rank, world, budget_s=150.0):
+    """The oracle as the reference arm: every step is a query sample of the
+    same workload, sized (from an untimed calibration step) so that warm-up
+    and timed steps together take about `budget_s` of host time."""
     if rank != 0:
         return
     inp = synth.make_layer(shape)
     labels = np.array(shape.mix, np.int8)
-    nq = 64
+    step = OracleStep(shape, inp, labels)
+    per_query = step(8, 999) / 8
+    nq = int(max(1, min(256, budget_s / max(1, args.steps + args.warmup) / per_query)))
     for s in range(args.warmup):
-        oracle_step_sample(shape, inp, labels, nq, 1000 + s)
+        step(nq, 1000 + s)
     t = 0.0
     for s in range(args.steps):
-        t += oracle_step_sample(shape, inp, labels, nq, s)
+        t += step(nq, s)
     value = nq * args.steps / t
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(shape),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                             "sample": f"{nq} query tokens per step (all heads, routed key sets)"},
+                             "sample": f"{nq} query tokens per step (all {shape.n_heads} heads, routed "
+                                       f"key sets) of the {shape.name} layer, fp64 NumPy"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
