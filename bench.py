@@ -289,6 +289,7 @@ class OracleStep:
 
     def __call__(self, n_queries, seed):
         ref = self.ref
+        n_queries = min(n_queries, self.n_q)
         idx = np.sort(np.random.default_rng(seed).choice(self.n_q, n_queries, replace=False))
         t0 = time.perf_counter()
         for h, a in enumerate(self.labels):
@@ -314,7 +315,7 @@ def blas_threads():
 def cpu_baseline(shape, inp, labels, seconds):
     """The oracle as it stands, on growing query samples until ~seconds of work."""
     step = OracleStep(shape, inp, labels)
-    done, spent, n = 0, 0.0, 16
+    done, spent, n = 0, 0.0, min(16, shape.n_q)
     seed = 0
     while spent < seconds:
         spent += step(n, seed)
@@ -336,7 +337,7 @@ def run_reference(args, shape, rank, world, budget_s=150.0):
     labels = np.array(shape.mix, np.int8)
     step = OracleStep(shape, inp, labels)
     per_query = step(8, 999) / 8
-    nq = int(max(1, min(256, budget_s / max(1, args.steps + args.warmup) / per_query)))
+    nq = int(max(1, min(256, shape.n_q, budget_s / max(1, args.steps + args.warmup) / per_query)))
     for s in range(args.warmup):
         step(nq, 1000 + s)
     t = 0.0
