@@ -448,6 +448,11 @@ hc_status hc_cache_create(const hc_config* cfg, const int8_t* labels_host, void*
     HC_CUDA(cudaMemcpy(static_cast<char*>(buf) + P.off_items, P.items.data(),
                        P.items.size() * sizeof(WorkItem), cudaMemcpyHostToDevice),
             "work-list upload");
+  // Clear the K/V areas: a run's last key tile reads past its filled ring
+  // slots while the window is still filling, and the masked probabilities
+  // (0) times uninitialised V rows could be 0 * NaN.
+  HC_CUDA(cudaMemset(static_cast<char*>(buf) + P.off_k, 0, P.bytes - P.off_k), "cache clear");
+  HC_CUDA(cudaStreamSynchronize(0), "cache clear");
   hc_cache* c = new hc_cache;
   std::memset(c, 0, sizeof *c);
   c->cfg = *cfg;
@@ -601,6 +606,7 @@ hc_status hc_full_attention(const hc_config* cfg, const void* q, const void* k, 
                             int32_t n_q_tokens, int32_t n_key_frames, void* o, void* stream) {
   hc_status s = hc_config_validate(cfg);
   if (s != HC_OK) return s;
+  if (n_q_tokens == 0) return HC_OK;   // nothing to compute; q and o may be null
   if (!q || !k || !v || !o) return fail(HC_ERR_INVALID_ARG, "null argument");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
     return fail(HC_ERR_ALIGN, "device pointers must be 16-byte aligned");

@@ -221,8 +221,10 @@ hc_status hc_classify_static_scratch(const hc_config* cfg, const void* q, const 
  *
  * hc_cache_bytes     bytes the buffer needs for these labels (HOST only).
  * hc_cache_create    binds a handle to `buf` (device, >= hc_cache_bytes,
- *                    256-byte aligned).  The caller keeps ownership of buf
- *                    and must keep it alive until hc_cache_destroy.
+ *                    256-byte aligned), writes the work list into it and
+ *                    clears its K/V areas (SYNC: waits for the clear).  The
+ *                    caller keeps ownership of buf and must keep it alive
+ *                    until hc_cache_destroy.
  * hc_cache_destroy   frees the handle only, never buf.
  * ------------------------------------------------------------------------- */
 hc_status hc_cache_bytes(const hc_config* cfg, const int8_t* labels_host, size_t* bytes);
@@ -262,7 +264,8 @@ hc_status hc_routed_attention(const hc_cache* cache, const void* q, void* o, voi
 
 /* Full attention of every head over [n_key_frames*F] monolithic keys: the
  * comparison path (and the warm-up path before classification).
- * q, o [Nq][H][d] with Nq = n_q_tokens; k, v [n_key_frames*F][H][d].  Async. */
+ * q, o [Nq][H][d] with Nq = n_q_tokens; k, v [n_key_frames*F][H][d].  Async.
+ * n_q_tokens = 0 is a no-op (the pointers may then be null). */
 hc_status hc_full_attention(const hc_config* cfg, const void* q, const void* k, const void* v,
                             int32_t n_q_tokens, int32_t n_key_frames, void* o, void* stream);
 
