@@ -231,20 +231,26 @@ def measured_peaks():
     return 1800.0, 6400.0, "fallback"
 
 
+KERNEL_SOURCES = ("attn_tc.cu", "hc_internal.h")   # the attention kernel's own code
+
+
+def kernel_source_hash():
+    import hashlib
+    src = os.path.join(ROOT, "head_routed_kv_classify_b300", "csrc")
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(src, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_from_profile(kernel_tag):
     """Per-launch DRAM bytes recorded by an ncu capture of the current kernel
-    source, or None if none matches."""
-    import hashlib
+    source (attn_tc.cu and hc_internal.h), or None if none matches."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, "head_routed_kv_classify_b300", "csrc")
-    h = hashlib.sha256()
-    for name in sorted(os.listdir(src)):
-        if name.endswith((".cu", ".h", ".cuh")):
-            with open(os.path.join(src, name), "rb") as f:
-                h.update(f.read())
-    digest = h.hexdigest()[:16]
+    digest = kernel_source_hash()
     tb, sha = None, None
     for line in open(path):
         if line.startswith("traffic_bytes_per_launch:"):
