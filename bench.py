@@ -901,6 +901,9 @@ def run_ours(args, shape, rank, world, local_rank):
                                 (total_ms / args.steps),
         "classify_ms": classify_ms, "restructure_ms": restructure_ms,
         "paths": paths,
+        "pages_context": {"end_to_end_generation_speedup_vs_full_attention": {"720P": 1.62, "1080P": 1.95},
+                          "hardware": "not stated on the pages",
+                          "note": "whole-model FPS ratios (LongLive, 30 s clips), not this metric"},
         "memory": hc.memory_report(cfg, labels),
         "wall_s_timed": wall,
     }

@@ -49,6 +49,12 @@ the design notes and used identically by the CUDA library):
   o12 cosine of two zero vectors is 1, of one zero vector 0;
   o15 a repeated block id overwrites the newest block; id+1 advances the
       window and evicts its oldest block.
+
+Parity unpinned: o1-o4 (how per-token cosines become a head's similarity, the
+composition of the score, the percentile definition) have no worked example
+on the pages, so no printed value pins them.  The arithmetic of each reading
+is pinned (tests/test_oracle.py: decision-rule boundaries, percentile and
+cosine/MSE closed forms); the readings themselves are not.
 """
 from __future__ import annotations
 
