@@ -840,35 +840,54 @@ def run_ours(args, shape, rank, world, local_rank):
     if not args.no_paths:
         paths = path_measurements(hc, shape, cfg, k, v, q, o, flush, stream, 10, peak_tf, peak_bw)
 
-    # End to end through the same public calls from pinned host buffers.
+    # End to end through the same public calls from pinned host buffers, as a
+    # caller would pipeline it: step i's Q/K/V copy in on one stream while
+    # step i-1 computes, and step i-1's output copies out on a third stream;
+    # every step's copies lie inside the timed region (first copy-in of the
+    # first timed step to the last copy-out).
     e2e = None
     if args.e2e_steps > 0:
         hq = [b.pin_memory() for b in (x.cpu() for x in qb)]
         hk = [b.pin_memory() for b in (x.cpu() for x in kb)]
         hv = [b.pin_memory() for b in (x.cpu() for x in vb)]
-        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(kb[0]), torch.empty_like(vb[0])
-        times = []
-        for i in range(args.warmup + args.e2e_steps):
-            flush.zero_()
-            a0, a1 = ev(), ev()
-            a0.record(stream)
-            dq.copy_(hq[i % 2], non_blocking=True)
-            dk.copy_(hk[i % 2], non_blocking=True)
-            dv.copy_(hv[i % 2], non_blocking=True)
-            cache.append(block_id(), dk, dv)
-            cache.routed_attention(dq, o)
-            ho.copy_(o, non_blocking=True)
-            a1.record(stream)
+        ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
+        dq = [torch.empty_like(q) for _ in range(2)]
+        dk = [torch.empty_like(kb[0]) for _ in range(2)]
+        dv = [torch.empty_like(vb[0]) for _ in range(2)]
+        do = [torch.empty_like(q) for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        n = args.warmup + args.e2e_steps
+        ev_in, ev_c, ev_out = [ev() for _ in range(n)], [ev() for _ in range(n)], [ev() for _ in range(n)]
+        t_start = ev()
+        for i in range(n):
+            b = i % 2
+            if i == args.warmup:
+                torch.cuda.synchronize()
+                t_start.record(s_in)
+            if i >= 2:
+                s_in.wait_event(ev_c[i - 2])          # buffers b free again
+            with torch.cuda.stream(s_in):
+                dq[b].copy_(hq[i % 2], non_blocking=True)
+                dk[b].copy_(hk[i % 2], non_blocking=True)
+                dv[b].copy_(hv[i % 2], non_blocking=True)
+            ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            if i >= 2:
+                stream.wait_event(ev_out[i - 2])      # do[b] copied out
+            cache.append(block_id(), dk[b], dv[b], stream=stream)
+            cache.routed_attention(dq[b], do[b], stream=stream)
+            ev_c[i].record(stream)
+            s_out.wait_event(ev_c[i])
+            with torch.cuda.stream(s_out):
+                ho[b].copy_(do[b], non_blocking=True)
+            ev_out[i].record(s_out)
             state["step"] += 1
-            if i >= args.warmup:
-                times.append((a0, a1))
         torch.cuda.synchronize()
-        times = [a.elapsed_time(b) for a, b in times]
+        e2e_ms = t_start.elapsed_time(ev_out[n - 1]) / args.e2e_steps
         nb = q.numel() * q.element_size()
-        e2e = {"value": world * shape.n_q / (1e-3 * statistics.mean(times)), "unit": UNIT,
-               "h2d_bytes_per_step": 3 * nb, "d2h_bytes_per_step": nb,
-               "ms_per_step": statistics.mean(times)}
+        e2e = {"value": world * shape.n_q / (1e-3 * e2e_ms), "unit": UNIT,
+               "h2d_bytes_per_step": 3 * nb, "d2h_bytes_per_step": nb, "ms_per_step": e2e_ms,
+               "pipelining": "copy-in, compute and copy-out of consecutive steps on three streams"}
 
     if rank != 0:
         return
