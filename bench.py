@@ -166,6 +166,23 @@ def job_value(units_per_rank_step, steps, max_ms, world):
     return world * units_per_rank_step * steps / (max_ms * 1e-3)
 
 
+def cache_kernel_rates(shape, labels, restructure_ms, append_ms, peak_bw):
+    """HBM rates of the cache kernels (bytes they must move / CUDA-event time):
+    the restructure reads the whole monolithic window and writes every head's
+    region; a steady-state append of a later block reads the block's K/V and
+    writes it for every head but the Sink heads (block 0 only)."""
+    row = 2 * shape.head_dim * 2                       # K and V of one (token, head), bf16
+    window_rows = shape.n_k * shape.n_heads
+    region_rows = sum(shape.n_q if a in (synth.SINK, synth.DUMMY) else shape.n_k for a in labels)
+    restructure_b = row * (window_rows + region_rows)
+    append_b = row * (shape.n_q * shape.n_heads + shape.n_q * sum(1 for a in labels if a != synth.SINK))
+    out = {}
+    for name, b, ms in (("restructure", restructure_b, restructure_ms), ("append", append_b, append_ms)):
+        gbs = b / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "bytes": b, "gbs": gbs, "frac_hbm": gbs / peak_bw}
+    return out
+
+
 class ClockSampler:
     """nvidia-smi samples taken while the timed region runs."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -919,6 +936,9 @@ def run_ours(args, shape, rank, world, local_rank):
         "step_speedup_vs_full": (statistics.mean(full_ms) + statistics.mean(mono_ms)) /
                                 (total_ms / args.steps),
         "classify_ms": classify_ms, "restructure_ms": restructure_ms,
+        "cache_kernels": cache_kernel_rates(shape, labels, restructure_ms,
+                                            statistics.mean(s - r for s, r in zip(step_ms, routed_ms)),
+                                            peak_bw),
         "paths": paths,
         "pages_context": {"end_to_end_generation_speedup_vs_full_attention": {"720P": 1.62, "1080P": 1.95},
                           "hardware": "not stated on the pages",
