@@ -778,12 +778,23 @@ template <int D, bool PROXY>
 cudaError_t launch_d(const TcArgs& a, dim3 grid, cudaStream_t s) {
   constexpr int smem = Layout<D>::ALLOC;
   static_assert(smem <= 232448, "shared memory budget");
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(attn_tc_kernel<D, PROXY>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  });
-  if (attr != cudaSuccess) return attr;
+  // The dynamic shared-memory opt-in is a per-device attribute of the
+  // function: set it once on every device the process launches on.
+  constexpr int kMaxDevices = 128;
+  static std::mutex mu;
+  static bool configured[kMaxDevices] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      e = cudaFuncSetAttribute(attn_tc_kernel<D, PROXY>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      configured[dev] = true;
+    }
+  }
   attn_tc_kernel<D, PROXY><<<grid, NTHREADS, smem, s>>>(a);
   return cudaGetLastError();
 }
