@@ -224,6 +224,22 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr0, uint32_t taddr1, ui
       : "r"(taddr0), "r"(taddr1)
       : "memory");
 }
+// 64 consecutive TMEM columns of this thread's lane together with their
+// maximum, reduced by the load itself (tcgen05.ld.red), so that a tile
+// without masked keys needs no max instructions.
+__device__ __forceinline__ float tmem_ld64_max(uint32_t taddr, uint32_t* r) {
+  float m;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x64.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,"
+      "%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, %64, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : HC_R32_8(0), HC_R32_8(8), HC_R32_8(16), HC_R32_8(24), HC_R32_8(32), HC_R32_8(40), HC_R32_8(48),
+        HC_R32_8(56), "=f"(m)
+      : "r"(taddr)
+      : "memory");
+  return m;
+}
 #undef HC_R32
 #define HC_W32(i) "r"(r[i])
 #define HC_W32_8(b) HC_W32(b), HC_W32(b + 1), HC_W32(b + 2), HC_W32(b + 3), HC_W32(b + 4), HC_W32(b + 5), \
@@ -598,30 +614,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
           }
         }
       }
-      // Pass 1: row max over the tile (8 independent partial maxima,
-      // three-input max).
+      // Pass 1: row max over the tile.  Without masked keys the TMEM load
+      // reduces it; otherwise 8 independent partial maxima (three-input max)
+      // over the masked values.
       float pm[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+      if (!PROXY && full) {
 #pragma unroll
-      for (int h = 0; h < BN / 64; ++h) {
-        uint32_t x[64];
-        tmem_ld32x2(t_s + h * 64, t_s + h * 64 + 32, x);
-        if (PROXY) {
-#pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (!((mw[2 * h + e / 32] >> (e & 31)) & 1u)) x[e] = __float_as_uint(-INFINITY);
-        } else if (!full) {
-#pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
+        for (int h = 0; h < BN / 64; ++h) {
+          uint32_t x[64];
+          pm[h] = tmem_ld64_max(t_s + h * 64, x);
         }
+      } else {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          pm[u] = max3f(pm[u], __uint_as_float(x[8 * u]), __uint_as_float(x[8 * u + 1]));
-          pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 2]), __uint_as_float(x[8 * u + 3]));
-          pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 4]), __uint_as_float(x[8 * u + 5]));
-          pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 6]), __uint_as_float(x[8 * u + 7]));
+        for (int h = 0; h < BN / 64; ++h) {
+          uint32_t x[64];
+          tmem_ld32x2(t_s + h * 64, t_s + h * 64 + 32, x);
+          if (PROXY) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (!((mw[2 * h + e / 32] >> (e & 31)) & 1u)) x[e] = __float_as_uint(-INFINITY);
+          } else if (!full) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u]), __uint_as_float(x[8 * u + 1]));
+            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 2]), __uint_as_float(x[8 * u + 3]));
+            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 4]), __uint_as_float(x[8 * u + 5]));
+            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 6]), __uint_as_float(x[8 * u + 7]));
+          }
         }
       }
       pm[0] = max3f(pm[0], pm[1], pm[2]);
