@@ -17,7 +17,12 @@
 //              32-bit column) back over the first half of S_i and, when the
 //              max has grown by more than 2^8, rescales its row of O_i; at
 //              the end it normalises O_i and stores it.
-//   warp 8     TMA producer: K and V tiles into a 2-stage ring.
+//   warp 8     TMA producer: K and V tiles into 2-stage rings.  V(j) and
+//              K(j+1) travel together on one barrier, so the MMA issuer
+//              makes one data wait and one release commit per key tile:
+//              each barrier poll between two MMA batches leaves the tensor
+//              pipe idle, since an MMA issue returns only once the pipe
+//              accepts it.
 //   warp 9     MMA issuer, in the order P_0 V, S_0, P_1 V, S_1 per key tile,
 //              so the tensor core always has the other tile's products
 //              queued while a softmax group works.  S uses Q and K from
@@ -57,7 +62,7 @@ typedef __nv_bfloat16 bf16;
 constexpr int BM = 128;            // queries per tile (one MMA M)
 constexpr int QT = 2;              // query tiles per CTA
 constexpr int BN = 128;            // keys per tile
-constexpr int STAGES = 2;          // K/V ring depth
+constexpr int STAGES = 2;          // K and V ring depth
 constexpr int NTHREADS = 320;
 constexpr int W_PRODUCER = 8, W_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
@@ -83,9 +88,13 @@ struct Layout {
   static_assert(COL_O + QT * D <= TMEM_COLS, "TMEM budget");
 };
 
-// Barrier slots (8 bytes each) after OFF_BAR.
-enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_SFULL = 8, B_PFULL = 10,
-       B_ODONE = 12, B_FIN = 14, B_COUNT = 15 };
+// Barrier slots (8 bytes each) after OFF_BAR.  Tile j's loads travel in
+// load group j: V(j) and K(j+1) on one FULL barrier (K(0) alone on K0FULL);
+// one EMPTY commit after the last MMA of key tile j releases both stages.
+enum { B_K0FULL = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_SFULL = B_EMPTY + STAGES, B_PFULL = B_SFULL + QT,
+       B_ODONE = B_PFULL + QT, B_FIN = B_ODONE + QT, B_COUNT = B_FIN + 1 };
+// The barriers, the TMEM slot and the two flags fit the 256 bytes after OFF_BAR.
+static_assert(8 * B_COUNT + 12 <= 256, "barrier area");
 
 struct TcArgs {
   CUtensorMap tk;        // K as [rows][heads][D] (3-D map, box {64, 1, BN})
@@ -397,11 +406,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
   const int64_t HD = (int64_t)g.H * D;
 
   if (tid == 0) {
+    mbar_init(bar(B_K0FULL), 1);
     for (int st = 0; st < STAGES; ++st) {
-      mbar_init(bar(B_KFULL + st), 1);
-      mbar_init(bar(B_KEMPTY + st), 1);
-      mbar_init(bar(B_VFULL + st), 1);
-      mbar_init(bar(B_VEMPTY + st), 1);
+      mbar_init(bar(B_FULL + st), 1);
+      mbar_init(bar(B_EMPTY + st), 1);
     }
     for (int i = 0; i < QT; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
@@ -448,7 +456,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     // ---------------------------------------------------------------- producer
     if (lane == 0 && n_tiles > 0) {
       const int ycoord = args.kv_head_coord ? it.head : 0;
-      int issued_k = 0, issued_v = 0;
+      // First key row of tile t.
+      auto tile_row = [&](int t) -> int {
+        if (PROXY) {
+          const int f = t / it.tpf;
+          return (int)it.k_row0 + f * g.F + it.rlo * g.Fw + (t - f * it.tpf) * BN;
+        }
+        return (int)(it.k_row0 + (int64_t)t * BN);
+      };
+      auto load_tile = [&](uint32_t dst, const CUtensorMap* map, int t, uint32_t b) {
+#pragma unroll
+        for (int rgn = 0; rgn < L::NREG; ++rgn) tma_load_3d(dst + rgn * L::KV_REG, map, rgn * 64, ycoord, tile_row(t), b);
+      };
+      mbar_expect_tx(bar(B_K0FULL), L::KV_BYTES);
+      load_tile(sK, &args.tk, 0, bar(B_K0FULL));
+      int issued = 0;   // load groups issued
       bool stalled = false;
       for (int t = 0; t < n_tiles; ++t) {
         if (p.debug_stall && t >= 1) {
@@ -457,36 +479,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
           stalled = true;
           break;
         }
+        // Group t reuses V stage t % 2 and K stage (t + 1) % 2, which key
+        // tile t - 2's EMPTY commit releases (the MMA prologue's commit,
+        // counted as tile -1, releases K(0)).
         const int st = t % STAGES;
-        const uint32_t wpar = ((t / STAGES) - 1) & 1;
-        int row;
-        if (PROXY) {
-          const int f = t / it.tpf;
-          row = (int)it.k_row0 + f * g.F + it.rlo * g.Fw + (t - f * it.tpf) * BN;
-        } else {
-          row = (int)(it.k_row0 + (int64_t)t * BN);
-        }
-        if (t >= STAGES && !mbar_wait_bounded(bar(B_KEMPTY + st), wpar, abort_flag, wait_limit)) break;
-        mbar_expect_tx(bar(B_KFULL + st), L::KV_BYTES);
-#pragma unroll
-        for (int rgn = 0; rgn < L::NREG; ++rgn)
-          tma_load_3d(sK + st * L::KV_BYTES + rgn * L::KV_REG, &args.tk, rgn * 64, ycoord, row, bar(B_KFULL + st));
-        issued_k = t + 1;
-        if (t >= STAGES && !mbar_wait_bounded(bar(B_VEMPTY + st), wpar, abort_flag, wait_limit)) break;
-        mbar_expect_tx(bar(B_VFULL + st), L::KV_BYTES);
-#pragma unroll
-        for (int rgn = 0; rgn < L::NREG; ++rgn)
-          tma_load_3d(sV + st * L::KV_BYTES + rgn * L::KV_REG, &args.tv, rgn * 64, ycoord, row, bar(B_VFULL + st));
-        issued_v = t + 1;
+        if (t >= 1 && !mbar_wait_bounded(bar(B_EMPTY + st), ((t - 1) / 2) & 1, abort_flag, wait_limit)) break;
+        const bool knext = t + 1 < n_tiles;
+        mbar_expect_tx(bar(B_FULL + st), knext ? 2 * L::KV_BYTES : L::KV_BYTES);
+        load_tile(sV + st * L::KV_BYTES, &args.tv, t, bar(B_FULL + st));
+        if (knext) load_tile(sK + ((t + 1) % STAGES) * L::KV_BYTES, &args.tk, t + 1, bar(B_FULL + st));
+        issued = t + 1;
       }
-      if (stalled || *abort_flag || issued_v < n_tiles) {
+      if (stalled || *abort_flag || issued < n_tiles) {
         if (!stalled) *abort_flag = 1;
         // Let the copies still in flight land before the CTA's memory goes.
         volatile int zero_flag = 0;   // drains ignore the abort flag
-        for (int t = max(0, issued_k - STAGES); t < issued_k; ++t)
-          (void)mbar_wait_bounded(bar(B_KFULL + t % STAGES), (t / STAGES) & 1, &zero_flag, DRAIN_LIMIT_NS);
-        for (int t = max(0, issued_v - STAGES); t < issued_v; ++t)
-          (void)mbar_wait_bounded(bar(B_VFULL + t % STAGES), (t / STAGES) & 1, &zero_flag, DRAIN_LIMIT_NS);
+        (void)mbar_wait_bounded(bar(B_K0FULL), 0, &zero_flag, DRAIN_LIMIT_NS);
+        for (int t = max(0, issued - STAGES); t < issued; ++t)
+          (void)mbar_wait_bounded(bar(B_FULL + t % STAGES), (t / STAGES) & 1, &zero_flag, DRAIN_LIMIT_NS);
       }
     }
     __syncwarp();
@@ -525,38 +535,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
           mma_bf16_ts(tmem + L::COL_O + i * D, tmem + i * BN + ks * 8, dv + ((ks * 16 * 128) >> 4), ID_PV,
                       (j > 0 || ks > 0) ? 1u : 0u);
       };
-      bool ok = wait1(B_KFULL, 0);
+      bool ok = wait1(B_K0FULL, 0);
       if (ok) {
         tc_fence_after();
         mma_s(0, 0);
         if (two) mma_s(1, 0);
-        mma_commit(bar(B_KEMPTY));
+        mma_commit(bar(B_EMPTY + 1));   // tile -1: releases K(0)
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j % STAGES;
-        const int nst = (j + 1) % STAGES;
         const bool more = j + 1 < n_tiles;
-        if (!(ok = wait1(B_VFULL + st, (j / STAGES) & 1))) break;
+        // V(j) and K(j+1) arrive together.
+        if (!(ok = wait1(B_FULL + st, (j / STAGES) & 1))) break;
         if (!(ok = wait1(B_PFULL + 0, j & 1))) break;
         tc_fence_after();
         mma_pv(0, j);
-        if (!two) mma_commit(bar(B_VEMPTY + st));
-        if (more) {
-          if (!(ok = wait1(B_KFULL + nst, ((j + 1) / STAGES) & 1))) break;
-          tc_fence_after();
-          mma_s(0, j + 1);
-          if (!two) mma_commit(bar(B_KEMPTY + nst));
-        }
+        if (more) mma_s(0, j + 1);
         if (two) {
           if (!(ok = wait1(B_PFULL + 1, j & 1))) break;
           tc_fence_after();
           mma_pv(1, j);
-          mma_commit(bar(B_VEMPTY + st));
-          if (more) {
-            mma_s(1, j + 1);
-            mma_commit(bar(B_KEMPTY + nst));
-          }
+          if (more) mma_s(1, j + 1);
         }
+        mma_commit(bar(B_EMPTY + st));   // releases V(j) and K(j+1)
       }
       if (ok) {
         mma_commit(bar(B_ODONE + 0));
