@@ -91,7 +91,9 @@ struct Layout {
 // Barrier slots (8 bytes each) after OFF_BAR.  Tile j's loads travel in
 // load group j: V(j) and K(j+1) on one FULL barrier (K(0) alone on K0FULL);
 // one EMPTY commit after the last MMA of key tile j releases both stages.
-enum { B_K0FULL = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_SFULL = B_EMPTY + STAGES, B_PFULL = B_SFULL + QT,
+// S_0 has its own barrier (SFULL); S_1(j) is signalled by the EMPTY commit
+// that follows it, which tracks the same MMAs.
+enum { B_K0FULL = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_SFULL = B_EMPTY + STAGES, B_PFULL = B_SFULL + 1,
        B_ODONE = B_PFULL + QT, B_FIN = B_ODONE + QT, B_COUNT = B_FIN + 1 };
 // The barriers, the TMEM slot and the two flags fit the 256 bytes after OFF_BAR.
 static_assert(8 * B_COUNT + 12 <= 256, "barrier area");
@@ -411,8 +413,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       mbar_init(bar(B_FULL + st), 1);
       mbar_init(bar(B_EMPTY + st), 1);
     }
+    mbar_init(bar(B_SFULL), 1);
     for (int i = 0; i < QT; ++i) {
-      mbar_init(bar(B_SFULL + i), 1);
       mbar_init(bar(B_PFULL + i), 4);   // one arrival per softmax warp
       mbar_init(bar(B_ODONE + i), 1);
     }
@@ -525,7 +527,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
           const uint32_t qoff = (ks >> 2) * L::Q_REG + ((ks & 3) << 5);
           mma_bf16_ss(tmem + i * BN, dq + (qoff >> 4), dk + (koff >> 4), ID_S, ks > 0 ? 1u : 0u);
         }
-        mma_commit(bar(B_SFULL + i));
+        if (i == 0) mma_commit(bar(B_SFULL));   // S_1: the EMPTY commit right after it
       };
       // O_i += P_i(j) V(j), P_i from the first half of S_i's columns.
       auto mma_pv = [&](int i, int j) {
@@ -592,7 +594,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       return __all_sync(0xffffffffu, w);
     };
     for (int j = 0; active && j < n_tiles; ++j) {
-      if (!wait_warp(B_SFULL + grp, j & 1)) { ok = false; break; }
+      // S_1(j) is signalled by key tile j-1's EMPTY commit (the MMA
+      // prologue's for j = 0): slot (j+1) % 2, its (j/2)-th completion.
+      const int s_slot = grp == 0 ? (int)B_SFULL : B_EMPTY + (j + 1) % STAGES;
+      if (!wait_warp(s_slot, grp == 0 ? (j & 1) : ((j / 2) & 1))) { ok = false; break; }
       tc_fence_after();
       const int valid = min(BN, it.k_len - j * BN);
       const bool full = PROXY || valid == BN;   // only a key run's last tile is partial
