@@ -773,12 +773,19 @@ def run_ours(args, shape, rank, world, local_rank):
     if list(labels) != list(shape.mix):
         raise RuntimeError(f"classification gave {list(labels)}, planted {list(shape.mix)}")
     cache = hc.hc_cache_create(cfg, labels, device=dev)
-    flush.zero_()
-    e0.record(stream)
-    cache.restructure(k, v, 0)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    restructure_ms = e0.elapsed_time(e1)
+    # Restructuring the same window again rewrites the same rows: two untimed
+    # calls, then the median of five, each after an L2 flush.
+    for _ in range(2):
+        cache.restructure(k, v, 0)
+    restructure_times = []
+    for _ in range(5):
+        flush.zero_()
+        e0.record(stream)
+        cache.restructure(k, v, 0)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        restructure_times.append(e0.elapsed_time(e1))
+    restructure_ms = float(np.median(restructure_times))
 
     # Steady-state inputs: two fresh blocks alternate (4 denoising steps per block).
     blocks = [synth.make_block(shape, seed=shape.seed + 77 + i + 1000 * rank) for i in range(2)]
