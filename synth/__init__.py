@@ -179,12 +179,13 @@ def make_layer(shape: LayerShape, seed: int | None = None, mix=None) -> LayerInp
                        _store(v, shape.dtype), mix)
 
 
-def make_block(shape: LayerShape, seed: int, mix=None, planted_dirs=None):
+def make_block(shape: LayerShape, seed: int, mix=None):
     """Fresh Q, K, V for one 3-frame block (a steady-state denoising step).
 
-    Planted heads keep their structure: Sink/Dummy queries get the same
-    directions as at classification time when ``planted_dirs`` is given, and
-    Spatial heads the same feature map (derived from ``seed`` otherwise)."""
+    All values are fresh N(0, 1) draws from ``seed``; Spatial heads also get a
+    positional plant (a feature map drawn from the same generator, queries
+    4*c*s and keys c*s).  Sink and Dummy heads get no plant here (streams
+    whose plants persist across blocks come from ``make_stream``)."""
     mix = tuple(shape.mix if mix is None else mix)
     rng = np.random.default_rng(seed)
     H, d, F = shape.n_heads, shape.head_dim, shape.frame_tokens

@@ -294,6 +294,39 @@ def test_cache_model_ring():
         cache.put(6, *blk(6))
 
 
+def _scipy_attention(q, k, v, scale):
+    """softmax(q k^T * scale) v through scipy's softmax (not the oracle's)."""
+    return scipy.special.softmax((q @ k.T) * scale, axis=1) @ v
+
+
+def test_routed_sink_and_dummy_read_block_zero_and_the_newest_block():
+    """Routed Sink heads attend over the block put with id 0 (kept after the
+    window has slid past it), Dummy heads over the newest block (after an
+    overwrite, its latest contents), Global heads over the window only.
+    Swapping any two of these key sets in the oracle fails here."""
+    geom = ref.Geometry(3, 4, 2, 3, 6, cell_h=1, cell_w=1)   # 2 blocks per window, 6-token blocks
+    rng = np.random.default_rng(12)
+    blocks = {b: (rng.standard_normal((6, 3, 4)), rng.standard_normal((6, 3, 4))) for b in range(5)}
+    cache = ref.CacheModel(geom)
+    for b in range(4):
+        cache.put(b, *blocks[b])
+    cache.put(4, *blocks[4])
+    newest = (rng.standard_normal((6, 3, 4)), rng.standard_normal((6, 3, 4)))
+    cache.put(4, *newest)                                     # a later denoising step of block 4
+    q = rng.standard_normal((6, 3, 4))
+    scale = 1 / math.sqrt(4)
+    labels = [ref.SINK, ref.DUMMY, ref.GLOBAL]
+    out = ref.routed_attention(q, cache, labels)
+    win_k = np.concatenate([blocks[3][0], newest[0]])
+    win_v = np.concatenate([blocks[3][1], newest[1]])
+    for h, (k, v) in enumerate([blocks[0], newest, (win_k, win_v)]):
+        want = _scipy_attention(q[:, h], k[:, h], v[:, h], scale)
+        assert np.max(np.abs(out[:, h] - want)) < 1e-12, h
+    # and they differ from one another on these inputs
+    assert np.max(np.abs(_scipy_attention(q[:, 0], blocks[0][0][:, 0], blocks[0][1][:, 0], scale) -
+                         _scipy_attention(q[:, 0], newest[0][:, 0], newest[1][:, 0], scale))) > 1e-2
+
+
 # ---------------------------------------------------------------- inputs
 
 def test_bf16_rounding_matches_torch():
