@@ -147,9 +147,14 @@ def test_routed_and_full_sampled_full_size(name):
     cache.restructure(k, v, 0)
     o = gu.to_host(cache.routed_attention(q))
     of = gu.to_host(hc.hc_full_attention(cfg, q, k, v))
+    # Sink, Dummy and Global heads on a seeded sample; Spatial heads on one
+    # query for every frame row of every cell.
     idx = gu.sample_queries(shape.n_q, 48, seed=shape.seed)
-    want = ref.routed_attention(inp.q.values, cache_ref, labels, query_idx=idx)
-    gu.assert_close(o[idx], want, "bf16", f"{name} routed sample")
+    cells = gu.per_cell_row_sample(shape, seed=shape.seed + 5)
+    for h, a in enumerate(labels):
+        qi = cells if a == ref.SPATIAL else idx
+        want = ref.routed_head(inp.q.values, cache_ref, int(a), h, query_idx=qi)
+        gu.assert_close(o[qi, h], want, "bf16", f"{name} routed head {h} ({a})")
     idx2 = gu.sample_queries(shape.n_q, 16, seed=shape.seed + 100)
     want_f = ref.full_attention(inp.q.values, inp.k.values, inp.v.values, query_idx=idx2)
     gu.assert_close(of[idx2], want_f, "bf16", f"{name} full sample")
