@@ -35,7 +35,7 @@ STATUS_NAMES = {0: "HC_OK", 1: "HC_ERR_INVALID_ARG", 2: "HC_ERR_SHAPE", 3: "HC_E
                 4: "HC_ERR_ALIGN", 5: "HC_ERR_STATE", 6: "HC_ERR_CUDA", 7: "HC_ERR_TIMEOUT",
                 8: "HC_ERR_UNSUPPORTED", 9: "HC_ERR_SIZE"}
 MAX_HEADS = 64
-ABI_VERSION = 3                   # HC_ABI_VERSION this binding is written against
+ABI_VERSION = 4                   # HC_ABI_VERSION this binding is written against
 STATIC_SCRATCH_BYTES = 16 << 20   # HC_STATIC_SCRATCH_BYTES
 
 # Every symbol include/headcast.h declares.
@@ -43,7 +43,7 @@ EXPORTS = ("hc_abi_version", "hc_status_string", "hc_last_error_message", "hc_co
            "hc_config_validate", "hc_classify_scratch_bytes", "hc_classify", "hc_cache_bytes",
            "hc_cache_create", "hc_cache_destroy", "hc_cache_get_info", "hc_cache_restructure",
            "hc_cache_append", "hc_routed_attention", "hc_full_attention", "hc_get_last_error",
-           "hc_classify_static_scratch", "hc_debug_inject_stall")
+           "hc_classify_static_scratch", "hc_debug_inject_stall", "hc_cache_plan_info")
 
 
 class HeadcastUnavailable(RuntimeError):
@@ -79,7 +79,16 @@ class HcCacheInfo(C.Structure):
     _fields_ = [("newest_block", C.c_int64), ("valid_frames", C.c_int32),
                 ("sink_present", C.c_int32), ("n_by_archetype", C.c_int32 * 4),
                 ("rows_by_archetype", C.c_int64 * 4), ("bytes", C.c_size_t),
+                ("kv_bytes", C.c_size_t), ("split_bytes", C.c_size_t),
                 ("monolithic_bytes", C.c_size_t)]
+
+    def as_dict(self) -> dict:
+        return dict(newest_block=self.newest_block, valid_frames=self.valid_frames,
+                    sink_present=bool(self.sink_present),
+                    n_by_archetype=list(self.n_by_archetype),
+                    rows_by_archetype=list(self.rows_by_archetype), bytes=self.bytes,
+                    kv_bytes=self.kv_bytes, split_bytes=self.split_bytes,
+                    monolithic_bytes=self.monolithic_bytes)
 
 
 _lib = None
@@ -107,6 +116,7 @@ def load(path: str = LIB_PATH):
         "hc_cache_create": (C.c_int, [cfgp, vp, vp, sz, C.POINTER(vp)]),
         "hc_cache_destroy": (C.c_int, [vp]),
         "hc_cache_get_info": (C.c_int, [vp, C.POINTER(HcCacheInfo)]),
+        "hc_cache_plan_info": (C.c_int, [cfgp, vp, C.POINTER(HcCacheInfo)]),
         "hc_cache_restructure": (C.c_int, [vp, vp, vp, i64, i32, vp]),
         "hc_cache_append": (C.c_int, [vp, i64, vp, vp, vp]),
         "hc_routed_attention": (C.c_int, [vp, vp, vp, vp]),
@@ -297,11 +307,7 @@ class Cache:
     def info(self) -> dict:
         inf = HcCacheInfo()
         _check(load().hc_cache_get_info(self.handle, C.byref(inf)))
-        return dict(newest_block=inf.newest_block, valid_frames=inf.valid_frames,
-                    sink_present=bool(inf.sink_present),
-                    n_by_archetype=list(inf.n_by_archetype),
-                    rows_by_archetype=list(inf.rows_by_archetype), bytes=inf.bytes,
-                    monolithic_bytes=inf.monolithic_bytes)
+        return inf.as_dict()
 
     def restructure(self, k_win, v_win, first_block_id=0, n_blocks=None, stream=None):
         cfg = self.cfg
@@ -361,21 +367,27 @@ def hc_get_last_error(stream=None):
 
 # ----------------------------------------------------------------- host-side helpers
 
+def hc_cache_plan_info(cfg, labels) -> dict:
+    """What hc_cache_create would reserve for these labels (host only)."""
+    lab = np.ascontiguousarray(np.asarray(labels, dtype=np.int8))
+    inf = HcCacheInfo()
+    _check(load().hc_cache_plan_info(C.byref(cfg), lab.ctypes.data_as(C.c_void_p), C.byref(inf)))
+    return inf.as_dict()
+
+
 def memory_report(cfg, labels) -> dict:
     """Steady-state KV-cache footprint of one layer for these labels against
-    the monolithic [window][H][d] K/V cache, from hc_cache_bytes (host only).
+    the monolithic [window][H][d] K/V cache, as the library plans it
+    (hc_cache_plan_info, host only).  `ratio` compares the K/V regions with
+    the monolithic cache; `bytes` is the whole backing store (K/V regions,
+    work list and schedule, and the split-run workspace).
     [Pith review of HeadCast, Figure 9 caption / Appendix C: memory of the
     restructured cache.]"""
-    lab = np.asarray(labels, dtype=np.int8)
-    esize = 2 if cfg.dtype == HC_BF16 else 4
-    F, d = cfg.F, cfg.head_dim
-    rows = {ARCHETYPES[a]: 0 for a in range(4)}
-    for a in lab:
-        rows[ARCHETYPES[int(a)]] += (cfg.frames_per_block if a in (SINK, DUMMY) else cfg.window_frames) * F
-    total = hc_cache_bytes(cfg, lab)
-    mono = 2 * cfg.window_frames * F * cfg.n_heads * d * esize
-    return {"bytes": total, "kv_bytes": 2 * sum(rows.values()) * d * esize, "monolithic_bytes": mono,
-            "ratio": total / mono, "rows_by_archetype": rows}
+    info = hc_cache_plan_info(cfg, labels)
+    rows = {ARCHETYPES[a]: int(info["rows_by_archetype"][a]) for a in range(4)}
+    return {"bytes": info["bytes"], "kv_bytes": info["kv_bytes"], "split_bytes": info["split_bytes"],
+            "monolithic_bytes": info["monolithic_bytes"],
+            "ratio": info["kv_bytes"] / info["monolithic_bytes"], "rows_by_archetype": rows}
 
 
 _LETTERS = "SDPG"

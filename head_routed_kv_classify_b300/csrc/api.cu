@@ -6,8 +6,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <map>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -15,6 +17,7 @@
 
 using hc::Geom;
 using hc::HeadSlot;
+using hc::SplitItem;
 using hc::WorkItem;
 
 // Device status word: kernels record bounded-wait expiry or a failed bounds
@@ -27,9 +30,13 @@ struct hc_cache {
   int8_t labels[HC_MAX_HEADS];
   HeadSlot heads[HC_MAX_HEADS];
   char* buf;
-  size_t bytes, used, off_items, off_k, off_v;
+  size_t bytes, used, off_items, off_sched, off_split, off_k, off_v, off_part_o, off_part_ml;
   int n_items;
   int n_band;            // trailing band items (sliding Spatial heads), launched separately
+  int n_cta_main, n_cta_band;
+  int n_split;           // split key runs merged after the launch
+  size_t split_bytes;    // partial-output workspace of the split runs
+  hc::PatchGeom pg;      // patches of the sliding Spatial heads (tensor-core path)
   int64_t rows;
   int64_t rows_by_arch[4];
   int n_by_arch[4];
@@ -117,13 +124,20 @@ int64_t head_rows(const Geom& g, int arch) {
 }
 
 struct Plan {
-  std::vector<WorkItem> items;
+  std::vector<WorkItem> items;       // main items in CTA order, then band items in CTA order
+  std::vector<int32_t> sched_main;   // CTA c of the main launch: items [sched[c], sched[c+1])
+  std::vector<int32_t> sched_band;   // the same for the band launch (offsets into the band items)
+  std::vector<SplitItem> splits;
   int n_band = 0;
+  int n_parts = 0;
   HeadSlot heads[HC_MAX_HEADS];
   int64_t rows = 0;
   int64_t rows_by_arch[4] = {0, 0, 0, 0};
   int n_by_arch[4] = {0, 0, 0, 0};
-  size_t off_items = 0, off_k = 0, off_v = 0, bytes = 0;
+  size_t off_items = 0, off_sched = 0, off_split = 0, off_k = 0, off_v = 0, off_part_o = 0, off_part_ml = 0;
+  size_t bytes = 0, split_bytes = 0;
+  hc::PatchGeom pg;      // patches of the sliding Spatial heads (tensor-core path)
+  bool ok = true;        // false: no patch geometry fits the sliding window
 };
 
 hc_status check_labels(const hc_config* cfg, const int8_t* labels) {
@@ -134,11 +148,97 @@ hc_status check_labels(const hc_config* cfg, const int8_t* labels) {
   return HC_OK;
 }
 
-// Cache layout and the routed work list.  The hardware block scheduler
-// dispatches items in list order.
+constexpr int kKeyTile = 128;   // keys per tile of the tensor-core kernel
+constexpr int kMaxChunks = 8;   // most pieces a key run is split into
+constexpr int kItemOverhead = 6;   // an item boundary, in key-tile steps (measured: about 8 us)
+
+// Key tiles of an item with the window full (the steady state), plus the
+// item boundary: the cost the schedule balances.
+int64_t item_cost(const Geom& g, const WorkItem& w, const hc::PatchGeom* pg = nullptr) {
+  int64_t keys;
+  if (w.kind == hc::ITEM_PATCH && pg) return (int64_t)g.Wf * pg->tpf + kItemOverhead;
+  if (w.kind == hc::ITEM_BAND) {
+    int lo, rhi, wl, wh, rlo;
+    const int t0 = w.q0 % g.F;
+    hc::band_window(g, hc::WIN_SLIDING, t0 / g.Fw, 0, rlo, rhi, wl, wh);
+    hc::band_window(g, hc::WIN_SLIDING, (t0 + w.nq - 1) / g.Fw, 0, lo, rhi, wl, wh);
+    const int64_t tpf = ((int64_t)(rhi - rlo + 1) * g.Fw + kKeyTile - 1) / kKeyTile;
+    return (int64_t)g.Wf * tpf + kItemOverhead;
+  }
+  keys = w.k_per_frame > 0 ? (int64_t)w.k_per_frame * g.Wf : w.k_len;
+  const int64_t tiles = (keys + kKeyTile - 1) / kKeyTile;
+  return (w.n_chunks > 1 ? (tiles + w.n_chunks - 1) / w.n_chunks : tiles) + kItemOverhead;
+}
+
+int64_t run_tiles(const Geom& g, const WorkItem& w) {
+  const int64_t keys = w.k_per_frame > 0 ? (int64_t)w.k_per_frame * g.Wf : w.k_len;
+  return (keys + kKeyTile - 1) / kKeyTile;
+}
+
+// Finishing time of the busiest CTA when items of these costs are dealt
+// longest-first to `ctas` CTAs, each to the least loaded one.
+int64_t lpt_makespan(std::vector<int64_t> costs, int ctas) {
+  std::sort(costs.begin(), costs.end(), std::greater<int64_t>());
+  std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> heap;
+  for (int c = 0; c < ctas; ++c) heap.push(0);
+  int64_t span = 0;
+  for (int64_t x : costs) {
+    const int64_t l = heap.top() + x;
+    heap.pop();
+    heap.push(l);
+    span = std::max(span, l);
+  }
+  return span;
+}
+
+// Longest-processing-time-first assignment of items to `ctas` CTAs: items in
+// decreasing cost, each to the CTA with the least work so far.  Returns the
+// items regrouped per CTA (each CTA's in assignment order) and the ranges.
+void lpt_schedule(const Geom& g, std::vector<WorkItem>& items, int max_ctas, std::vector<int32_t>& sched,
+                  const hc::PatchGeom* pg = nullptr) {
+  const int n = (int)items.size();
+  const int ctas = std::max(1, std::min(max_ctas, n));
+  std::vector<int> order(n);
+  for (int i = 0; i < n; ++i) order[i] = i;
+  std::vector<int64_t> cost(n);
+  for (int i = 0; i < n; ++i) cost[i] = item_cost(g, items[i], pg);
+  // Equal costs keep their list order, so items that read the same key run
+  // (adjacent in the list) go to neighbouring CTAs and run at the same time,
+  // and all but the first read the run from L2.
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+  typedef std::pair<int64_t, int> Load;   // (work so far, cta)
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int c = 0; c < ctas; ++c) heap.push(Load(0, c));
+  std::vector<std::vector<int>> lists(ctas);
+  for (int i : order) {
+    Load l = heap.top();
+    heap.pop();
+    lists[l.second].push_back(i);
+    heap.push(Load(l.first + cost[i], l.second));
+  }
+  std::vector<WorkItem> out;
+  out.reserve(n);
+  sched.assign(ctas + 1, 0);
+  for (int c = 0; c < ctas; ++c) {
+    sched[c] = (int32_t)out.size();
+    for (int i : lists[c]) out.push_back(items[i]);
+  }
+  sched[ctas] = (int32_t)out.size();
+  items.swap(out);
+}
+
+// Cache layout, the routed work list and its schedule.
 void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
   const Geom g = make_geom(cfg);
   const int BM = hc::attention_block_rows(cfg.dtype, cfg.head_dim);
+  std::vector<WorkItem> main, band;
+  std::memset(&P.pg, 0, sizeof P.pg);
+  const bool patches = cfg.dtype == HC_BF16 && g.spatial_mode == HC_SPATIAL_SLIDING;
+  if (patches) {
+    bool any = false;
+    for (int h = 0; h < g.H; ++h) any = any || labels[h] == HC_SPATIAL;
+    if (any && !hc::choose_patch_geom(g, hc::WIN_SLIDING, g.Wf, P.pg)) P.ok = false;
+  }
   for (int h = 0; h < g.H; ++h) {
     const int a = labels[h];
     P.heads[h].arch = a;
@@ -148,7 +248,8 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
     P.rows += r;
     P.rows_by_arch[a] += r;
     P.n_by_arch[a] += 1;
-    auto push = [&](int kind, int q0, int nq, int64_t k_row0, int k_len, int k_per_frame, int cell) {
+    auto push = [&](std::vector<WorkItem>& list, int kind, int q0, int nq, int64_t k_row0, int k_len,
+                    int k_per_frame, int cell) {
       WorkItem w;
       std::memset(&w, 0, sizeof w);
       w.head = h;
@@ -160,20 +261,27 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
       w.k_per_frame = k_per_frame;
       w.cell = cell;
       w.out_plane = 0;
-      P.items.push_back(w);
+      w.chunk = 0;
+      w.n_chunks = 1;
+      w.part = -1;
+      list.push_back(w);
     };
     if (a == HC_SINK || a == HC_DUMMY) {
       for (int q0 = 0; q0 < g.blk; q0 += BM)
-        push(hc::ITEM_RANGE, q0, std::min(BM, g.blk - q0), P.heads[h].row0, g.blk, 0, 0);
+        push(main, hc::ITEM_RANGE, q0, std::min(BM, g.blk - q0), P.heads[h].row0, g.blk, 0, 0);
     } else if (a == HC_GLOBAL) {
       for (int q0 = 0; q0 < g.blk; q0 += BM)
-        push(hc::ITEM_RANGE, q0, std::min(BM, g.blk - q0), P.heads[h].row0, 0, g.F, 0);
+        push(main, hc::ITEM_RANGE, q0, std::min(BM, g.blk - q0), P.heads[h].row0, 0, g.F, 0);
+    } else if (g.spatial_mode == HC_SPATIAL_SLIDING && patches) {
+      // Patches of query positions (in every frame of the block); the kernel
+      // reads each patch's halo as boxes and masks each query's window.
+      for (int k = 0; k < P.pg.n; ++k) push(band, hc::ITEM_PATCH, 0, 0, P.heads[h].row0, 0, g.F, k);
     } else if (g.spatial_mode == HC_SPATIAL_SLIDING) {
       // Runs of up to BM tokens inside one frame of the block; the kernel
       // derives the band of window rows and masks each query's window.
       for (int f = 0; f < g.fpb; ++f)
         for (int t0 = 0; t0 < g.F; t0 += BM)
-          push(hc::ITEM_BAND, f * g.F + t0, std::min(BM, g.F - t0), P.heads[h].row0, 0, g.F, 0);
+          push(band, hc::ITEM_BAND, f * g.F + t0, std::min(BM, g.F - t0), P.heads[h].row0, 0, g.F, 0);
     } else {
       for (int ci = 0; ci < g.ncell_h; ++ci)
         for (int cj = 0; cj < g.ncell_w; ++cj) {
@@ -182,44 +290,92 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
           const int csz = hz * wz, nq = g.fpb * csz;
           const int64_t k0 = P.heads[h].row0 + (int64_t)g.Wf * hc::cell_tokens_before(g, ci, cj);
           for (int q0 = 0; q0 < nq; q0 += BM)
-            push(hc::ITEM_CELL, q0, std::min(BM, nq - q0), k0, 0, csz, ci * g.ncell_w + cj);
+            push(main, hc::ITEM_CELL, q0, std::min(BM, nq - q0), k0, 0, csz, ci * g.ncell_w + cj);
         }
     }
   }
-  // Order: groups of items that read the same key run (one head's block or
-  // window run, or one Spatial cell of one head) stay adjacent, so that the
-  // CTAs sharing a run execute together and all but the first read it from
-  // L2; groups go longest-first (by their total work) and, inside a group,
-  // items go longest-first.
-  auto cost = [&](const WorkItem& w) {
-    const int64_t keys = w.k_per_frame > 0 ? (int64_t)w.k_per_frame * g.Wf : w.k_len;
-    return keys * w.nq;
-  };
-  auto group = [&](const WorkItem& w) -> int64_t {
-    return (int64_t)w.head * (1 << 20) + (w.kind == hc::ITEM_CELL ? w.cell + 1 : 0);
-  };
-  // Band items go last, as their own launch of the masked kernel variant.
-  std::stable_partition(P.items.begin(), P.items.end(),
-                        [](const WorkItem& w) { return w.kind != hc::ITEM_BAND; });
-  const auto band0 = std::find_if(P.items.begin(), P.items.end(),
-                                  [](const WorkItem& w) { return w.kind == hc::ITEM_BAND; });
-  P.n_band = (int)(P.items.end() - band0);
-  std::map<int64_t, int64_t> group_cost;
-  for (const WorkItem& w : P.items) group_cost[group(w)] += cost(w);
-  auto order = [&](const WorkItem& x, const WorkItem& y) {
-    const int64_t gx = group(x), gy = group(y);
-    const int64_t cx = group_cost[gx], cy = group_cost[gy];
-    if (cx != cy) return cx > cy;
-    if (gx != gy) return gx < gy;
-    return cost(x) > cost(y);
-  };
-  std::stable_sort(P.items.begin(), band0, order);
-  std::stable_sort(band0, P.items.end(), order);
+  if (cfg.dtype == HC_BF16 && !main.empty()) {
+    // Split-KV: the longest key runs (Sink, Dummy or Global items) are cut
+    // into pieces whose partial outputs are merged after the launch, as long
+    // as that shortens the launch's busiest CTA by more than 5 %: it
+    // removes both a single item that outlasts the rest of the launch and
+    // the quantisation of a few long items over the CTAs.
+    const int n = (int)main.size();
+    std::vector<int> chunks(n, 1), best = chunks;
+    auto costs = [&](const std::vector<int>& ch) {
+      std::vector<int64_t> c;
+      for (int i = 0; i < n; ++i) {
+        const int64_t t = main[i].kind == hc::ITEM_RANGE ? run_tiles(g, main[i]) : item_cost(g, main[i]) - kItemOverhead;
+        // A piece of a split run also writes its partial output and is read
+        // back by the merge: one more step.
+        for (int k = 0; k < ch[i]; ++k) c.push_back((t + ch[i] - 1) / ch[i] + kItemOverhead + (ch[i] > 1 ? 1 : 0));
+      }
+      return c;
+    };
+    int64_t best_span = lpt_makespan(costs(chunks), hc::kPlanCtas);
+    for (int iter = 0; iter < 4 * kMaxChunks; ++iter) {
+      // One more piece for every splittable item among the longest pieces.
+      int64_t top = 0;
+      for (int i = 0; i < n; ++i)
+        if (main[i].kind == hc::ITEM_RANGE && chunks[i] < kMaxChunks)
+          top = std::max(top, (run_tiles(g, main[i]) + chunks[i] - 1) / chunks[i]);
+      if (top < 8) break;   // pieces of under 8 key tiles are not worth a merge
+      bool grew = false;
+      for (int i = 0; i < n; ++i)
+        if (main[i].kind == hc::ITEM_RANGE && chunks[i] < kMaxChunks &&
+            (run_tiles(g, main[i]) + chunks[i] - 1) / chunks[i] * 100 >= top * 97) {
+          ++chunks[i];
+          grew = true;
+        }
+      if (!grew) break;
+      const int64_t span = lpt_makespan(costs(chunks), hc::kPlanCtas);
+      if (span * 100 < best_span * 95) {
+        best_span = span;
+        best = chunks;
+      }
+    }
+    std::vector<WorkItem> split;
+    for (int i = 0; i < n; ++i) {
+      const WorkItem& w = main[i];
+      const int k = best[i];
+      if (k <= 1) {
+        split.push_back(w);
+        continue;
+      }
+      SplitItem si;
+      std::memset(&si, 0, sizeof si);
+      si.head = w.head;
+      si.q0 = w.q0;
+      si.nq = w.nq;
+      si.n_chunks = k;
+      si.part0 = P.n_parts;
+      P.splits.push_back(si);
+      for (int c = 0; c < k; ++c) {
+        WorkItem x = w;
+        x.chunk = (int16_t)c;
+        x.n_chunks = (int16_t)k;
+        x.part = P.n_parts + c;
+        split.push_back(x);
+      }
+      P.n_parts += k;
+    }
+    main.swap(split);
+  }
+  lpt_schedule(g, main, hc::kPlanCtas, P.sched_main);
+  if (!band.empty()) lpt_schedule(g, band, hc::kPlanCtas, P.sched_band, &P.pg);
+  P.n_band = (int)band.size();
+  P.items = main;
+  P.items.insert(P.items.end(), band.begin(), band.end());
   const size_t row_bytes = (size_t)g.d * esize_of(cfg.dtype);
   P.off_items = 256;
-  P.off_k = round_up(P.off_items + P.items.size() * sizeof(WorkItem), 256);
+  P.off_sched = round_up(P.off_items + P.items.size() * sizeof(WorkItem), 256);
+  P.off_split = round_up(P.off_sched + 2 * (hc::kMaxCtas + 1) * sizeof(int32_t), 256);
+  P.off_k = round_up(P.off_split + P.splits.size() * sizeof(SplitItem), 256);
   P.off_v = round_up(P.off_k + (size_t)P.rows * row_bytes, 256);
-  P.bytes = round_up(P.off_v + (size_t)P.rows * row_bytes, 256);
+  P.off_part_o = round_up(P.off_v + (size_t)P.rows * row_bytes, 256);
+  P.off_part_ml = round_up(P.off_part_o + (size_t)P.n_parts * hc::kPartRows * g.d * sizeof(float), 256);
+  P.bytes = round_up(P.off_part_ml + (size_t)P.n_parts * hc::kPartRows * 2 * sizeof(float), 256);
+  P.split_bytes = P.bytes - P.off_part_o;
 }
 
 }  // namespace
@@ -313,12 +469,31 @@ hc_status hc_config_validate(const hc_config* c) {
 
 // ------------------------------------------------------------ classification
 
-static void classify_layout(const hc_config& c, size_t* planes, size_t* tok, size_t* total) {
+// Classification workspace.  bf16 layers (tensor-core path): the proxy
+// output plane, the two parked states of the fused pass and their row
+// max / sum, and the per-token statistics.  fp32 layers: four output planes
+// (full, Sink, Dummy, proxy) and the per-token statistics.
+struct ClassifyLayout {
+  size_t plane, off_proxy, off_park, off_park_ml, off_tok, total;
+};
+
+static ClassifyLayout classify_layout(const hc_config& c) {
   const int64_t nq = (int64_t)c.frames_per_block * c.frame_h * c.frame_w;
-  const size_t plane = (size_t)nq * c.n_heads * c.head_dim * sizeof(float);
-  *planes = plane;
-  *tok = round_up(4 * plane, 256);
-  *total = round_up(*tok + 4 * (size_t)c.n_heads * nq * sizeof(float), 256);
+  ClassifyLayout L;
+  L.plane = (size_t)nq * c.n_heads * c.head_dim * sizeof(float);
+  const size_t tok = 4 * (size_t)c.n_heads * nq * sizeof(float);
+  if (c.dtype == HC_BF16) {
+    L.off_proxy = 0;
+    L.off_park = round_up(L.plane, 256);
+    L.off_park_ml = round_up(L.off_park + 2 * L.plane, 256);
+    L.off_tok = round_up(L.off_park_ml + 2 * (size_t)nq * c.n_heads * 2 * sizeof(float), 256);
+  } else {
+    L.off_proxy = 3 * L.plane;
+    L.off_park = L.off_park_ml = 0;
+    L.off_tok = round_up(4 * L.plane, 256);
+  }
+  L.total = round_up(L.off_tok + tok, 256);
+  return L;
 }
 
 hc_status hc_classify_scratch_bytes(const hc_config* cfg, int32_t n_key_frames, size_t* bytes) {
@@ -326,8 +501,7 @@ hc_status hc_classify_scratch_bytes(const hc_config* cfg, int32_t n_key_frames, 
   if (s != HC_OK) return s;
   if (!bytes) return fail(HC_ERR_INVALID_ARG, "bytes is null");
   (void)n_key_frames;
-  size_t pl, tk;
-  classify_layout(*cfg, &pl, &tk, bytes);
+  *bytes = classify_layout(*cfg).total;
   return HC_OK;
 }
 
@@ -346,9 +520,9 @@ hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const 
       n_key_frames > 4096)
     return fail(HC_ERR_SHAPE, "n_key_frames %d must be a multiple of frames_per_block and hold >= 2 blocks",
                 n_key_frames);
-  size_t plane, tok_off, need;
-  classify_layout(*cfg, &plane, &tok_off, &need);
-  if (scratch_bytes < need) return fail(HC_ERR_SIZE, "scratch %zu < %zu bytes", scratch_bytes, need);
+  const ClassifyLayout CL = classify_layout(*cfg);
+  if (scratch_bytes < CL.total) return fail(HC_ERR_SIZE, "scratch %zu < %zu bytes", scratch_bytes, CL.total);
+  char* sc = static_cast<char*>(scratch);
   int* status = nullptr;
   if ((s = status_ptr(&status)) != HC_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -361,36 +535,64 @@ hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const 
   p.q = q;
   p.k = k;
   p.v = v;
-  p.o = scratch;
   p.k_stride = (int64_t)g.H * g.d;
   p.k_hstride = g.d;
-  p.o_plane_stride = (int64_t)(plane / sizeof(float));
   p.nq_total = g.blk;
   p.out_fp32 = 1;
-  p.item_mode = hc::ITEMS_DENSE;
-  p.plane_k0[0] = 0;
-  p.plane_klen[0] = (int32_t)nk;
-  p.plane_k0[1] = 0;
-  p.plane_klen[1] = g.blk;
-  p.plane_k0[2] = nk - g.blk;
-  p.plane_klen[2] = g.blk;
   p.g = g;
   p.status = status;
   if (cfg->dtype == HC_BF16) {
     const hc::TcKV kv{k, v, g.H, nk};
-    HC_CUDA(hc::launch_attention_tc(p, kv, dim3((g.blk + BM - 1) / BM, g.H, 3), st), "classification attention");
+    // 1. The Spatial proxy output: patches of query positions with their
+    //    halo in every window frame (with the cell proxy: the deployed cells).
+    hc::AttnParams pp = p;
+    pp.item_mode = hc::ITEMS_PROXY;
+    pp.o = sc + CL.off_proxy;
+    pp.o_plane_stride = 0;
+    pp.proxy_frames = n_key_frames;
+    const bool pg_ok = g.proxy_mode == HC_PROXY_CELL ? hc::make_cell_patch_geom(g, pp.pg)
+                                                      : hc::choose_patch_geom(g, hc::WIN_PROXY, n_key_frames, pp.pg);
+    if (!pg_ok) return fail(HC_ERR_UNSUPPORTED, "the Spatial proxy window is too wide for the band kernel");
+    pp.band_win = hc::WIN_PROXY;
+    pp.n_items = g.H * pp.pg.n * pp.pg.cpc;
+    HC_CUDA(hc::launch_attention_tc(pp, kv, std::min(pp.n_items, hc::device_sm_count()), st),
+            "classification proxy attention");
+    // 2. One pass over all keys per query tile: the full-context output,
+    //    with the Sink block's and the current block's outputs taken from its
+    //    running state, and each token's cosines and squared error.
+    hc::AttnParams pc = p;
+    pc.item_mode = hc::ITEMS_DENSE;
+    pc.n_planes = 1;
+    pc.plane_k0[0] = 0;
+    pc.plane_klen[0] = (int32_t)nk;
+    pc.cls = 1;
+    pc.seg_sink = g.blk;
+    pc.seg_dummy = (int32_t)(nk - g.blk);
+    pc.park_o = reinterpret_cast<float*>(sc + CL.off_park);
+    pc.park_ml = reinterpret_cast<float*>(sc + CL.off_park_ml);
+    pc.proxy_o = reinterpret_cast<const float*>(sc + CL.off_proxy);
+    pc.tok = reinterpret_cast<float*>(sc + CL.off_tok);
+    pc.o_full = o_full;
+    pc.out_fp32 = 0;
+    pc.n_items = ((g.blk + BM - 1) / BM) * g.H;
+    HC_CUDA(hc::launch_attention_tc(pc, kv, std::min(pc.n_items, hc::device_sm_count()), st),
+            "classification attention");
   } else {
+    // fp32 layers: the four outputs as planes, then the statistics kernel.
+    p.o = scratch;
+    p.o_plane_stride = (int64_t)(CL.plane / sizeof(float));
+    p.item_mode = hc::ITEMS_DENSE;
+    p.n_planes = 3;
+    p.plane_k0[0] = 0;
+    p.plane_klen[0] = (int32_t)nk;
+    p.plane_k0[1] = 0;
+    p.plane_klen[1] = g.blk;
+    p.plane_k0[2] = nk - g.blk;
+    p.plane_klen[2] = g.blk;
     HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3((g.blk + BM - 1) / BM, g.H, 3), st),
             "classification attention");
-  }
-  p.item_mode = hc::ITEMS_PROXY;
-  p.proxy_frames = n_key_frames;
-  if (cfg->dtype == HC_BF16) {
-    p.tiles_per_frame = (g.F + BM - 1) / BM;
-    const hc::TcKV kv{k, v, g.H, nk};
-    HC_CUDA(hc::launch_attention_tc(p, kv, dim3(g.fpb * p.tiles_per_frame, g.H, 1), st),
-            "classification proxy attention");
-  } else {
+    p.item_mode = hc::ITEMS_PROXY;
+    p.proxy_frames = n_key_frames;
     const int PBM = hc::proxy_block_rows();
     p.tiles_per_frame = (g.F + PBM - 1) / PBM;
     HC_CUDA(hc::launch_attention(p, cfg->dtype, dim3(g.fpb * p.tiles_per_frame, g.H, 1), st),
@@ -400,8 +602,9 @@ hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const 
   hc::ClassifyPost c;
   std::memset(&c, 0, sizeof c);
   c.planes = static_cast<const float*>(scratch);
-  c.plane_stride = p.o_plane_stride;
-  c.tok = reinterpret_cast<float*>(static_cast<char*>(scratch) + tok_off);
+  c.plane_stride = (int64_t)(CL.plane / sizeof(float));
+  c.tok = reinterpret_cast<float*>(sc + CL.off_tok);
+  c.tokens_ready = cfg->dtype == HC_BF16 ? 1 : 0;   // the fused pass wrote them
   c.o_full = o_full;
   c.o_full_fp32 = cfg->dtype == HC_FP32;
   c.labels = labels_dev;
@@ -413,10 +616,18 @@ hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const 
   c.theta_spatial = cfg->theta_spatial;
   c.theta_score = cfg->theta_score;
   c.gamma = cfg->gamma;
+  c.status = status;
   HC_CUDA(hc::launch_classify_post(c, st), "classification statistics");
   if (labels_host) {
     HC_CUDA(cudaMemcpyAsync(labels_host, labels_dev, g.H, cudaMemcpyDeviceToHost, st), "label copy");
     HC_CUDA(cudaStreamSynchronize(st), "stream synchronize");
+    // A bounded wait that expired in any of the kernels leaves its mark in
+    // the status word (which stays set for hc_get_last_error): the labels
+    // were then not computed from complete outputs.
+    int word = 0;
+    HC_CUDA(cudaMemcpy(&word, status, sizeof word, cudaMemcpyDeviceToHost), "status read");
+    if (word == hc::DEV_TIMEOUT) return fail(HC_ERR_TIMEOUT, "a bounded device wait expired during classification");
+    if (word != hc::DEV_OK) return fail(HC_ERR_CUDA, "device status word %d", word);
   }
   return HC_OK;
 }
@@ -430,6 +641,9 @@ hc_status hc_cache_bytes(const hc_config* cfg, const int8_t* labels_host, size_t
   if (!bytes) return fail(HC_ERR_INVALID_ARG, "bytes is null");
   Plan P;
   plan_cache(*cfg, labels_host, P);
+  if (!P.ok)
+    return fail(HC_ERR_UNSUPPORTED, "the sliding Spatial window (%dx%d) is too wide for the band kernel", cfg->cell_h,
+                cfg->cell_w);
   *bytes = P.bytes;
   return HC_OK;
 }
@@ -443,15 +657,28 @@ hc_status hc_cache_create(const hc_config* cfg, const int8_t* labels_host, void*
   if ((reinterpret_cast<uintptr_t>(buf) & 255u) != 0) return fail(HC_ERR_ALIGN, "buf must be 256-byte aligned");
   Plan P;
   plan_cache(*cfg, labels_host, P);
+  if (!P.ok)
+    return fail(HC_ERR_UNSUPPORTED, "the sliding Spatial window (%dx%d) is too wide for the band kernel", cfg->cell_h,
+                cfg->cell_w);
   if (bytes < P.bytes) return fail(HC_ERR_SIZE, "buffer %zu < %zu bytes", bytes, P.bytes);
   if (!P.items.empty())
     HC_CUDA(cudaMemcpy(static_cast<char*>(buf) + P.off_items, P.items.data(),
                        P.items.size() * sizeof(WorkItem), cudaMemcpyHostToDevice),
             "work-list upload");
+  std::vector<int32_t> sched(2 * (hc::kMaxCtas + 1), 0);
+  std::copy(P.sched_main.begin(), P.sched_main.end(), sched.begin());
+  std::copy(P.sched_band.begin(), P.sched_band.end(), sched.begin() + hc::kMaxCtas + 1);
+  HC_CUDA(cudaMemcpy(static_cast<char*>(buf) + P.off_sched, sched.data(), sched.size() * sizeof(int32_t),
+                     cudaMemcpyHostToDevice),
+          "schedule upload");
+  if (!P.splits.empty())
+    HC_CUDA(cudaMemcpy(static_cast<char*>(buf) + P.off_split, P.splits.data(), P.splits.size() * sizeof(SplitItem),
+                       cudaMemcpyHostToDevice),
+            "split-table upload");
   // Clear the K/V areas: a run's last key tile reads past its filled ring
   // slots while the window is still filling, and the masked probabilities
   // (0) times uninitialised V rows could be 0 * NaN.
-  HC_CUDA(cudaMemset(static_cast<char*>(buf) + P.off_k, 0, P.bytes - P.off_k), "cache clear");
+  HC_CUDA(cudaMemset(static_cast<char*>(buf) + P.off_k, 0, P.off_part_o - P.off_k), "cache clear");
   HC_CUDA(cudaStreamSynchronize(0), "cache clear");
   hc_cache* c = new hc_cache;
   std::memset(c, 0, sizeof *c);
@@ -463,10 +690,19 @@ hc_status hc_cache_create(const hc_config* cfg, const int8_t* labels_host, void*
   c->bytes = bytes;
   c->used = P.bytes;
   c->off_items = P.off_items;
+  c->off_sched = P.off_sched;
+  c->off_split = P.off_split;
   c->off_k = P.off_k;
   c->off_v = P.off_v;
+  c->off_part_o = P.off_part_o;
+  c->off_part_ml = P.off_part_ml;
   c->n_items = (int)P.items.size();
   c->n_band = P.n_band;
+  c->n_cta_main = P.sched_main.empty() ? 0 : (int)P.sched_main.size() - 1;
+  c->n_cta_band = P.sched_band.empty() ? 0 : (int)P.sched_band.size() - 1;
+  c->n_split = (int)P.splits.size();
+  c->split_bytes = P.split_bytes;
+  c->pg = P.pg;
   c->rows = P.rows;
   for (int a = 0; a < 4; ++a) {
     c->rows_by_arch[a] = P.rows_by_arch[a];
@@ -484,6 +720,8 @@ hc_status hc_cache_destroy(hc_cache* cache) {
   return HC_OK;
 }
 
+static size_t kv_row_bytes(const hc_config& cfg) { return (size_t)cfg.head_dim * esize_of(cfg.dtype); }
+
 hc_status hc_cache_get_info(const hc_cache* c, hc_cache_info* out) {
   if (!c || !out) return fail(HC_ERR_INVALID_ARG, "null argument");
   std::memset(out, 0, sizeof *out);
@@ -495,7 +733,33 @@ hc_status hc_cache_get_info(const hc_cache* c, hc_cache_info* out) {
     out->rows_by_archetype[a] = c->rows_by_arch[a];
   }
   out->bytes = c->used;
+  out->kv_bytes = 2 * (size_t)c->rows * kv_row_bytes(c->cfg);
+  out->split_bytes = c->split_bytes;
   out->monolithic_bytes = (size_t)2 * c->g.Wf * c->g.F * c->g.H * c->g.d * esize_of(c->cfg.dtype);
+  return HC_OK;
+}
+
+hc_status hc_cache_plan_info(const hc_config* cfg, const int8_t* labels_host, hc_cache_info* out) {
+  hc_status s = hc_config_validate(cfg);
+  if (s != HC_OK) return s;
+  if ((s = check_labels(cfg, labels_host)) != HC_OK) return s;
+  if (!out) return fail(HC_ERR_INVALID_ARG, "out is null");
+  Plan P;
+  plan_cache(*cfg, labels_host, P);
+  if (!P.ok)
+    return fail(HC_ERR_UNSUPPORTED, "the sliding Spatial window (%dx%d) is too wide for the band kernel", cfg->cell_h,
+                cfg->cell_w);
+  const Geom g = make_geom(*cfg);
+  std::memset(out, 0, sizeof *out);
+  out->newest_block = -1;
+  for (int a = 0; a < 4; ++a) {
+    out->n_by_archetype[a] = P.n_by_arch[a];
+    out->rows_by_archetype[a] = P.rows_by_arch[a];
+  }
+  out->bytes = P.bytes;
+  out->kv_bytes = 2 * (size_t)P.rows * kv_row_bytes(*cfg);
+  out->split_bytes = P.split_bytes;
+  out->monolithic_bytes = (size_t)2 * g.Wf * g.F * g.H * g.d * esize_of(cfg->dtype);
   return HC_OK;
 }
 
@@ -581,18 +845,38 @@ hc_status hc_routed_attention(const hc_cache* c, const void* q, void* o, void* s
   p.g = c->g;
   p.status = status;
   if (c->cfg.dtype == HC_BF16) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
     const hc::TcKV kv{c->buf + c->off_k, c->buf + c->off_v, 1, c->rows};
+    const int32_t* sched = reinterpret_cast<const int32_t*>(c->buf + c->off_sched);
     const int n_main = c->n_items - c->n_band;
-    if (n_main > 0)
-      HC_CUDA(hc::launch_attention_tc(p, kv, dim3(n_main, 1, 1), static_cast<cudaStream_t>(stream)),
-              "routed attention");
+    p.part_o = reinterpret_cast<float*>(c->buf + c->off_part_o);
+    p.part_ml = reinterpret_cast<float*>(c->buf + c->off_part_ml);
+    if (n_main > 0) {
+      p.n_items = n_main;
+      p.sched = sched;
+      HC_CUDA(hc::launch_attention_tc(p, kv, c->n_cta_main, st), "routed attention");
+    }
     if (c->n_band > 0) {
       // Sliding Spatial heads: the masked band variant over the list's tail.
       p.items += n_main;
       p.n_items = c->n_band;
+      p.sched = sched + hc::kMaxCtas + 1;
       p.band_win = hc::WIN_SLIDING;
-      HC_CUDA(hc::launch_attention_tc(p, kv, dim3(c->n_band, 1, 1), static_cast<cudaStream_t>(stream)),
-              "routed attention (sliding Spatial)");
+      p.pg = c->pg;
+      HC_CUDA(hc::launch_attention_tc(p, kv, c->n_cta_band, st), "routed attention (sliding Spatial)");
+    }
+    if (c->n_split > 0) {
+      // Merge the split key runs' partial outputs.
+      hc::CombineParams m;
+      std::memset(&m, 0, sizeof m);
+      m.items = reinterpret_cast<const SplitItem*>(c->buf + c->off_split);
+      m.n_items = c->n_split;
+      m.out_fp32 = 0;
+      m.part_o = p.part_o;
+      m.part_ml = p.part_ml;
+      m.o = o;
+      m.g = c->g;
+      HC_CUDA(hc::launch_combine(m, st), "routed attention (split-run merge)");
     }
   } else {
     p.band_win = hc::WIN_SLIDING;
@@ -634,9 +918,13 @@ hc_status hc_full_attention(const hc_config* cfg, const void* q, const void* k, 
   p.g = g;
   p.status = status;
   const dim3 grid((n_q_tokens + BM - 1) / BM, g.H, 1);
+  p.n_planes = 1;
   if (cfg->dtype == HC_BF16) {
     const hc::TcKV kv{k, v, g.H, nk};
-    HC_CUDA(hc::launch_attention_tc(p, kv, grid, static_cast<cudaStream_t>(stream)), "full attention");
+    p.n_items = (int)(grid.x * grid.y);
+    HC_CUDA(hc::launch_attention_tc(p, kv, std::min(p.n_items, hc::device_sm_count()),
+                                    static_cast<cudaStream_t>(stream)),
+            "full attention");
   } else {
     HC_CUDA(hc::launch_attention(p, cfg->dtype, grid, static_cast<cudaStream_t>(stream)), "full attention");
   }

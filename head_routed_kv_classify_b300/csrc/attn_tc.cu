@@ -1,22 +1,25 @@
 // Softmax attention on the 5th-generation tensor cores (tcgen05 + TMEM),
 // with K/V tiles streamed by TMA.  Serves every bf16 attention of the
 // library: the routed pathways (Sink / Dummy / Global key runs and Spatial
-// cells of the restructured cache), the in-house full attention and the
-// full / Sink / Dummy planes of classification.
+// cells of the restructured cache, sliding Spatial patches), the in-house
+// full attention, and classification (the proxy, and one pass that yields
+// the full-context, Sink and Dummy outputs and the per-token statistics).
 // [Pith review of HeadCast: "The pith" and "Core claim" (each head attends
 //  only over its pathway), "What carries the argument" (the classification
 //  outputs), major comment 2 and Figure 3 caption (10x10 cells).]
 //
-// One CTA computes one work item: up to 256 queries of one head (two query
-// tiles of 128) against one contiguous run of key rows, streamed in tiles of
-// 128 keys.  Roles (320 threads):
+// A launch is persistent: each CTA runs a list of work items, each up to 256
+// queries of one head (two query tiles of 128) against one run of key rows
+// (or a patch's halo boxes), streamed in tiles of 128 keys.  Roles (320
+// threads):
 //   warps 0-3, 4-7  softmax groups, one per query tile: thread r of group i
 //              owns row r of tile i, i.e. TMEM lane r.  It reads its row of
 //              S_i = Q_i K^T from TMEM (a max pass, then an exponent pass),
 //              keeps the running max and sum, writes P_i (bf16, two per
 //              32-bit column) back over the first half of S_i and, when the
 //              max has grown by more than 2^8, rescales its row of O_i; at
-//              the end it normalises O_i and stores it.
+//              an item's end it gathers the next item's query rows and then
+//              normalises O_i and stores it.
 //   warp 8     TMA producer: K and V tiles into 2-stage rings.  V(j) and
 //              K(j+1) travel together on one barrier, so the MMA issuer
 //              makes one data wait and one release commit per key tile:
@@ -34,10 +37,12 @@
 // P_i(j-1) V(j-1), so a softmax group may rescale O_i as soon as it sees
 // S_i(j).
 // Band items -- the classification proxy (ITEMS_PROXY) and, with sliding
-// deployed Spatial heads, their routed items (ITEM_BAND) -- run the same
-// pipeline on the band of frame rows around a run of query tokens in every
-// frame, with a per-row window mask (the (2r+1) x (2r+1) neighbourhood, the
-// deployed cell, or the centred cell_h x cell_w window) applied to S.
+// deployed Spatial heads, their routed items (ITEM_PATCH) -- are patches of
+// query positions in every frame of the block: every query at a position
+// has the same key window, so a patch's keys in each key frame are its halo,
+// read as 2-D TMA boxes of a [frames][Fh][Fw][heads][d] view of K and V and
+// masked per query to its window (the (2r+1) x (2r+1) neighbourhood, the
+// deployed cell, or the centred cell_h x cell_w window).
 // Hand-offs are mbarriers; every wait is bounded in wall-clock time and on
 // expiry the CTA records HC_ERR_TIMEOUT in the status word, drains its own
 // copies and MMAs (again bounded), frees TMEM and returns.
@@ -67,6 +72,7 @@ constexpr int NTHREADS = 320;
 constexpr int W_PRODUCER = 8, W_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.f;  // rescale O when the row max grows by > 2^8
+constexpr int ITEM_CACHE = 256;    // work items of a CTA kept in shared memory
 constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;   // 1 s
 constexpr unsigned long long STALL_WAIT_LIMIT_NS = 2000000ull; // 2 ms under the stall test hook
 constexpr unsigned long long DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s
@@ -82,7 +88,8 @@ struct Layout {
   static constexpr int OFF_K = OFF_Q + QT * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
-  static constexpr int BYTES = OFF_BAR + 256;
+  static constexpr int OFF_ITEMS = OFF_BAR + 256;   // the CTA's work items (list launches)
+  static constexpr int BYTES = OFF_ITEMS + ITEM_CACHE * (int)sizeof(WorkItem);
   static constexpr int ALLOC = BYTES + 1024;        // room to align the base to 1 KB
   static constexpr uint32_t COL_O = QT * BN;        // O_i at COL_O + i * D
   static_assert(COL_O + QT * D <= TMEM_COLS, "TMEM budget");
@@ -94,7 +101,7 @@ struct Layout {
 // S_0 has its own barrier (SFULL); S_1(j) is signalled by the EMPTY commit
 // that follows it, which tracks the same MMAs.
 enum { B_K0FULL = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_SFULL = B_EMPTY + STAGES, B_PFULL = B_SFULL + 1,
-       B_ODONE = B_PFULL + QT, B_FIN = B_ODONE + QT, B_COUNT = B_FIN + 1 };
+       B_ODONE = B_PFULL + QT, B_QREADY = B_ODONE + QT, B_FIN = B_QREADY + QT, B_COUNT = B_FIN + 1 };
 // The barriers, the TMEM slot and the two flags fit the 256 bytes after OFF_BAR.
 static_assert(8 * B_COUNT + 12 <= 256, "barrier area");
 
@@ -157,6 +164,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// 16 bytes global -> shared without a register round trip; with
+// src_bytes = 0 nothing is read and the 16 bytes are zero-filled.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -169,6 +183,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            int c4, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], "
+      "[%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
       : "memory");
 }
 
@@ -304,72 +327,179 @@ struct TcItem {
   int64_t k_row0;
   int k_len;
   int h0, w0, hz, wz;   // ITEM_CELL: the cell
-  int rlo, rlen, tpf;   // band items: first band row, keys per frame band, key tiles per frame
+  int rlo, rlen, tpf;   // band items: halo origin row and column, key tiles (boxes) per key frame
+  int part;             // >= 0: partial output slot of a split key run
 };
 
-// Band of frame rows [h_lo(first row), h_hi(last row)] of a run of queries
-// [t0, t0 + nq) inside one frame, over `frames` frames of keys.
-__device__ __forceinline__ void tc_band(TcItem& it, const Geom& g, int win, int t0, int frames) {
-  const int hmin = t0 / g.Fw, hmax = (t0 + it.nq - 1) / g.Fw;
-  int lo, rhi, wl, wh;
-  band_window(g, win, hmin, 0, it.rlo, rhi, wl, wh);
-  band_window(g, win, hmax, 0, lo, rhi, wl, wh);
-  it.rlen = (rhi - it.rlo + 1) * g.Fw;
-  it.tpf = (it.rlen + BN - 1) / BN;
-  it.k_len = frames * it.tpf * BN;
+// A band item: patch `patch` of the launch's patch geometry, query chunk
+// `chunk`, over `frames` key frames.
+__device__ __forceinline__ void tc_patch(TcItem& it, const AttnParams& p, int patch, int chunk, int frames) {
+  const Geom& g = p.g;
+  const PatchGeom& pg = p.pg;
+  if (pg.cells) {
+    const int ci = patch / g.ncell_w, cj = patch - (patch / g.ncell_w) * g.ncell_w;
+    it.h0 = ci * g.cell_h;
+    it.hz = cell_extent(ci, g.Fh, g.cell_h, g.ncell_h);
+    it.w0 = cj * g.cell_w;
+    it.wz = cell_extent(cj, g.Fw, g.cell_w, g.ncell_w);
+  } else {
+    const int pi = patch / pg.npw, pj = patch - (patch / pg.npw) * pg.npw;
+    it.h0 = pi * pg.ph;
+    it.hz = min(pg.ph, g.Fh - it.h0);
+    it.w0 = pj * pg.pw;
+    it.wz = min(pg.pw, g.Fw - it.w0);
+  }
+  it.q0 = chunk * (QT * BM);
+  it.nq = min(QT * BM, g.fpb * it.hz * it.wz - it.q0);
+  it.rlo = it.h0 + pg.dh;
+  it.rlen = it.w0 + pg.dw;
+  it.tpf = pg.tpf;
+  it.k_len = it.nq > 0 ? frames * pg.tpf * BN : 0;
 }
 
-__device__ __forceinline__ TcItem tc_decode(const AttnParams& p) {
+// Work item w of the launch (`src`: where list launches read item w from).
+__device__ __forceinline__ TcItem tc_decode(const AttnParams& p, int w, const WorkItem* src) {
   const Geom& g = p.g;
   TcItem it;
   it.h0 = it.w0 = it.hz = it.wz = 0;
   it.rlo = it.rlen = it.tpf = 0;
+  it.part = -1;
   if (p.item_mode == ITEMS_PROXY) {
-    // Up to 256 consecutive tokens of one frame of the block; keys: the
-    // rows [h_min - r, h_max + r] of every window frame (one contiguous run
-    // of tokens per frame), narrowed per query by the neighbourhood mask.
-    const int f = blockIdx.x / p.tiles_per_frame, t0 = (blockIdx.x % p.tiles_per_frame) * (QT * BM);
-    it.head = blockIdx.y;
+    // A patch of query positions in every frame of the block (a query chunk
+    // of it with the cell proxy); keys: its halo in every window frame,
+    // narrowed per query to its window by the mask.
+    const int per_head = p.pg.n * p.pg.cpc;
+    const int x = w % per_head;
+    it.head = w / per_head;
     it.kind = ITEM_PROXY;
-    it.q0 = f * g.F + t0;
-    it.nq = min(QT * BM, g.F - t0);
     it.out_plane = 3;
     it.k_row0 = 0;
-    tc_band(it, g, WIN_PROXY, t0, p.proxy_frames);
+    tc_patch(it, p, x / p.pg.cpc, x % p.pg.cpc, p.proxy_frames);
   } else if (p.item_mode == ITEMS_LIST) {
-    const WorkItem w = p.items[blockIdx.x];
-    it.head = w.head;
-    it.kind = w.kind;
-    it.q0 = w.q0;
-    it.nq = w.nq;
-    it.out_plane = w.out_plane;
-    it.k_row0 = w.k_row0;
-    it.k_len = w.k_per_frame > 0 ? w.k_per_frame * p.valid_frames : w.k_len;
-    if (w.kind == ITEM_CELL) {
-      const int ci = w.cell / g.ncell_w, cj = w.cell % g.ncell_w;
+    const WorkItem wi = *src;
+    it.head = wi.head;
+    it.kind = wi.kind;
+    it.q0 = wi.q0;
+    it.nq = wi.nq;
+    it.out_plane = wi.out_plane;
+    it.k_row0 = wi.k_row0;
+    it.k_len = wi.k_per_frame > 0 ? wi.k_per_frame * p.valid_frames : wi.k_len;
+    if (wi.kind == ITEM_CELL) {
+      const int ci = wi.cell / g.ncell_w, cj = wi.cell % g.ncell_w;
       it.h0 = ci * g.cell_h;
       it.hz = cell_extent(ci, g.Fh, g.cell_h, g.ncell_h);
       it.w0 = cj * g.cell_w;
       it.wz = cell_extent(cj, g.Fw, g.cell_w, g.ncell_w);
-    } else if (w.kind == ITEM_BAND) {
-      // Sliding Spatial: the head's ring slots in raster order from k_row0.
-      tc_band(it, g, p.band_win, w.q0 % g.F, p.valid_frames);
+    } else if (wi.kind == ITEM_PATCH) {
+      // Sliding Spatial: patch wi.cell; keys in the head's filled ring slots,
+      // stored in raster order from row k_row0.
+      tc_patch(it, p, wi.cell, 0, p.valid_frames);
     }
-  } else {  // ITEMS_DENSE
-    it.head = blockIdx.y;
+    if (wi.n_chunks > 1 && wi.kind != ITEM_PATCH) {
+      // This item's share of the run's T key tiles (possibly none while the
+      // window is still filling); the run's last, partial tile stays last.
+      const int T = (it.k_len + BN - 1) / BN;
+      const int t0 = (int)((int64_t)wi.chunk * T / wi.n_chunks);
+      const int t1 = (int)((int64_t)(wi.chunk + 1) * T / wi.n_chunks);
+      it.k_row0 += (int64_t)t0 * BN;
+      it.k_len = t1 > t0 ? min(it.k_len - t0 * BN, (t1 - t0) * BN) : 0;
+    }
+    it.part = wi.part;
+  } else {  // ITEMS_DENSE: w = ((plane * H) + head) * n_q_tiles + q_tile
+    const int nx = (p.nq_total + QT * BM - 1) / (QT * BM);
+    const int x = w % nx, rest = w / nx;
+    const int z = rest / g.H;
+    it.head = rest - z * g.H;
     it.kind = ITEM_RANGE;
-    it.q0 = blockIdx.x * (QT * BM);
+    it.q0 = x * (QT * BM);
     it.nq = min(QT * BM, p.nq_total - it.q0);
-    it.out_plane = blockIdx.z;
-    it.k_row0 = p.plane_k0[blockIdx.z];
-    it.k_len = p.plane_klen[blockIdx.z];
+    it.out_plane = z;
+    it.k_row0 = p.plane_k0[z];
+    it.k_len = p.plane_klen[z];
   }
   return it;
 }
 
-// Block-local token of the r-th query of an item.
+// Classification full pass: key tiles of the Sink and middle segments (the
+// Dummy segment's follow).
+__device__ __forceinline__ int cls_n0(const AttnParams& p) { return (p.seg_sink + BN - 1) / BN; }
+__device__ __forceinline__ int cls_n1(const AttnParams& p) { return (p.seg_dummy - p.seg_sink + BN - 1) / BN; }
+
+__device__ __forceinline__ int tc_tiles(const AttnParams& p, const TcItem& it, bool cls) {
+  if (it.k_len <= 0) return 0;
+  if (cls) return cls_n0(p) + cls_n1(p) + (it.k_len - p.seg_dummy + BN - 1) / BN;
+  return (it.k_len + BN - 1) / BN;
+}
+
+// First key row and valid keys of key tile j (segments of the
+// classification pass each end in their own partial tile).
+__device__ __forceinline__ void tile_span(const AttnParams& p, bool cls, int64_t k_row0, int k_len, int j, int& row,
+                                          int& valid) {
+  if (cls) {
+    const int n0 = cls_n0(p), n1 = cls_n1(p);
+    int a, b;
+    if (j < n0) {
+      a = 0;
+      b = p.seg_sink;
+    } else if (j < n0 + n1) {
+      a = p.seg_sink;
+      b = p.seg_dummy;
+      j -= n0;
+    } else {
+      a = p.seg_dummy;
+      b = k_len;
+      j -= n0 + n1;
+    }
+    row = (int)k_row0 + a + j * BN;
+    valid = min(BN, b - a - j * BN);
+    return;
+  }
+  row = (int)k_row0 + j * BN;
+  valid = min(BN, k_len - j * BN);
+}
+
+// The items of this CTA: w0, w0 + step, ... below w1.
+__device__ __forceinline__ void cta_items(const AttnParams& p, int& w0, int& w1, int& step) {
+  if (p.sched) {
+    w0 = p.sched[blockIdx.x];
+    w1 = p.sched[blockIdx.x + 1];
+    step = 1;
+  } else {
+    w0 = blockIdx.x;
+    w1 = p.n_items;
+    step = gridDim.x;
+  }
+}
+
+// The CTA's list items: the first ITEM_CACHE from shared memory, the rest
+// (of an unusually long list) from global memory.
+struct ItemSrc {
+  const WorkItem* smem;   // null: nothing staged
+  const WorkItem* gmem;
+  int w0;
+  __device__ __forceinline__ const WorkItem* at(int w) const {
+    return smem && w - w0 < ITEM_CACHE ? smem + (w - w0) : gmem + w;
+  }
+};
+
+__device__ __forceinline__ TcItem tc_decode(const AttnParams& p, int w, const ItemSrc& src) {
+  return tc_decode(p, w, p.item_mode == ITEMS_LIST ? src.at(w) : nullptr);
+}
+
+// First item at or after w with at least one key (w1 if none).
+__device__ __forceinline__ int next_keyed(const AttnParams& p, int w, int w1, int step, const ItemSrc& src,
+                                          TcItem& it) {
+  for (; w < w1; w += step) {
+    it = tc_decode(p, w, src);
+    if (it.k_len > 0) return w;
+  }
+  return w1;
+}
+
+// Block-local token of the r-th query of an item (cells and patches: query
+// ordinals in (frame, row, column) order inside the cell or patch).
 __device__ __forceinline__ int tc_query_token(const TcItem& it, const Geom& g, int r) {
-  if (it.kind != ITEM_CELL) return it.q0 + r;
+  if (it.kind == ITEM_RANGE) return it.q0 + r;
   const int ord = it.q0 + r;
   const int csz = it.hz * it.wz;
   const int fq = ord / csz, rem = ord - fq * csz;
@@ -378,8 +508,22 @@ __device__ __forceinline__ int tc_query_token(const TcItem& it, const Geom& g, i
 }
 
 // ---------------------------------------------------------------- the kernel
+//
+// Persistent: each CTA runs its items back to back with one TMEM allocation
+// and one set of barriers.  The key tiles of all its items form one global
+// sequence g = 0, 1, ...: load group g carries V(g) and K(g+1), where K(g+1)
+// may be the first key tile of the next item, so the producer runs ahead
+// across item boundaries.  At a boundary each softmax group, once it has
+// consumed S_i of the item's last tile, gathers its query tile of the next
+// item into shared memory (arrival on QREADY_i) and then stores the item's
+// output (after ODONE_i); the MMA issuer issues the next item's first S_i as
+// soon as QREADY_i arrives, so the epilogue overlaps the next item's start.
+// Every item runs both query tiles (rows past the item's queries are zero
+// and never stored), so both softmax groups see every key tile.
 
-template <int D, bool PROXY>
+// PROXY: band items (masked halo boxes); CLS: the classification pass
+// (segmented keys, parked states, per-token statistics).
+template <int D, bool PROXY, bool CLS>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ TcArgs args) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -395,17 +539,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
   const AttnParams& p = args.p;
   const Geom& g = p.g;
   const unsigned long long wait_limit = p.wait_limit_ns;
+  int w_begin, w_end, w_step;
+  cta_items(p, w_begin, w_end, w_step);
   // Once any CTA has recorded an expired wait, the rest of the launch (and
   // later launches, until the status word is read and cleared) skip their
   // work so that a broken pipeline fails fast.
   if (threadIdx.x == 0) *skip_flag = p.status ? *reinterpret_cast<volatile int*>(p.status) : 0;
   __syncthreads();
-  if (*skip_flag) return;
-  const TcItem it = tc_decode(p);
+  if (*skip_flag || w_begin >= w_end) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_tiles = it.k_len > 0 ? (it.k_len + BN - 1) / BN : 0;
-  const bool two = it.nq > BM;   // second query tile in use
   const int64_t HD = (int64_t)g.H * D;
+  const bool staged = p.item_mode == ITEMS_LIST && w_step == 1;
+  const ItemSrc isrc{staged ? reinterpret_cast<const WorkItem*>(smem + L::OFF_ITEMS) : nullptr, p.items, w_begin};
+  if (PROXY) {
+    // A band tile's box fills only its first bh*kw key rows; the rest of the
+    // K and V stages must hold finite values (their probabilities are 0, and
+    // 0 times a stale NaN would not be), so they start as zeros.
+    int4* kv = reinterpret_cast<int4*>(smem + L::OFF_K);
+    for (int i = tid; i < 2 * STAGES * L::KV_BYTES / 16; i += NTHREADS) kv[i] = make_int4(0, 0, 0, 0);
+    fence_proxy_async();   // before the tensor core and TMA touch them
+  }
+  if (staged) {
+    // Stage this CTA's items in shared memory: every role decodes each item
+    // several times, and a decode must not wait on global memory at an item
+    // boundary.  (List launches run a contiguous range: w_step == 1.)
+    const int n = min(w_end - w_begin, ITEM_CACHE) * (int)(sizeof(WorkItem) / 16);
+    const int4* src = reinterpret_cast<const int4*>(p.items + w_begin);
+    int4* dst = reinterpret_cast<int4*>(smem + L::OFF_ITEMS);
+    for (int i = tid; i < n; i += NTHREADS) dst[i] = src[i];
+  }
 
   if (tid == 0) {
     mbar_init(bar(B_K0FULL), 1);
@@ -415,8 +577,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     }
     mbar_init(bar(B_SFULL), 1);
     for (int i = 0; i < QT; ++i) {
-      mbar_init(bar(B_PFULL + i), 4);   // one arrival per softmax warp
+      mbar_init(bar(B_PFULL + i), 4);    // one arrival per softmax warp
       mbar_init(bar(B_ODONE + i), 1);
+      mbar_init(bar(B_QREADY + i), 4);   // one arrival per softmax warp
     }
     mbar_init(bar(B_FIN), 1);
     *abort_flag = 0;
@@ -432,23 +595,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&args.tk)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&args.tv)) : "memory");
   }
-  if (warp < 4 * QT) {
-    // Query tiles: thread r of group i loads row i*128 + r of the item
-    // (zeros past its queries) into the K-major 128-byte-swizzled layout.
-    const int grp = warp >> 2, r = tid & 127, qrow = grp * BM + r;
-    const bool ok = qrow < it.nq;
-    const int tok = ok ? tc_query_token(it, g, qrow) : 0;
-    const int4* src = reinterpret_cast<const int4*>(static_cast<const bf16*>(p.q) + tok * HD + (int64_t)it.head * D);
-    const uint32_t q_tile = sQ + grp * L::Q_BYTES;
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      int4 v = ok ? __ldg(src + c) : make_int4(0, 0, 0, 0);
-      const uint32_t dst = q_tile + (c >> 3) * L::Q_REG + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                   : "memory");
-    }
-    fence_proxy_async();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -456,47 +602,72 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
 
   if (warp == W_PRODUCER) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0 && n_tiles > 0) {
-      const int ycoord = args.kv_head_coord ? it.head : 0;
-      // First key row of tile t.
-      auto tile_row = [&](int t) -> int {
+    if (lane == 0) {
+      auto load_tile = [&](uint32_t dst, const CUtensorMap* map, const TcItem& it, int t, uint32_t b) {
+        const int y = args.kv_head_coord ? it.head : 0;
         if (PROXY) {
-          const int f = t / it.tpf;
-          return (int)it.k_row0 + f * g.F + it.rlo * g.Fw + (t - f * it.tpf) * BN;
-        }
-        return (int)(it.k_row0 + (int64_t)t * BN);
-      };
-      auto load_tile = [&](uint32_t dst, const CUtensorMap* map, int t, uint32_t b) {
+          // Box tt of key frame f of the item's halo: bh rows x kw columns
+          // from (rlo + tt*bh, rlen), read as a [frames][Fh][Fw][heads][d]
+          // tensor (zeros outside the frame).
+          const int f = t / it.tpf, tt = t - f * it.tpf;
+          const int fr = p.band_frame0 + (int)(it.k_row0 / g.F) + f;
 #pragma unroll
-        for (int rgn = 0; rgn < L::NREG; ++rgn) tma_load_3d(dst + rgn * L::KV_REG, map, rgn * 64, ycoord, tile_row(t), b);
-      };
-      mbar_expect_tx(bar(B_K0FULL), L::KV_BYTES);
-      load_tile(sK, &args.tk, 0, bar(B_K0FULL));
-      int issued = 0;   // load groups issued
-      bool stalled = false;
-      for (int t = 0; t < n_tiles; ++t) {
-        if (p.debug_stall && t >= 1) {
-          // Test hook: stop feeding without raising the abort flag, so that
-          // the consumers' bounded waits expire.
-          stalled = true;
-          break;
+          for (int rgn = 0; rgn < L::NREG; ++rgn)
+            tma_load_5d(dst + rgn * L::KV_REG, map, rgn * 64, y, it.rlen, it.rlo + tt * p.pg.bh, fr, b);
+          return;
         }
-        // Group t reuses V stage t % 2 and K stage (t + 1) % 2, which key
-        // tile t - 2's EMPTY commit releases (the MMA prologue's commit,
-        // counted as tile -1, releases K(0)).
-        const int st = t % STAGES;
-        if (t >= 1 && !mbar_wait_bounded(bar(B_EMPTY + st), ((t - 1) / 2) & 1, abort_flag, wait_limit)) break;
-        const bool knext = t + 1 < n_tiles;
-        mbar_expect_tx(bar(B_FULL + st), knext ? 2 * L::KV_BYTES : L::KV_BYTES);
-        load_tile(sV + st * L::KV_BYTES, &args.tv, t, bar(B_FULL + st));
-        if (knext) load_tile(sK + ((t + 1) % STAGES) * L::KV_BYTES, &args.tk, t + 1, bar(B_FULL + st));
-        issued = t + 1;
+        int z, vz;
+        tile_span(p, CLS, it.k_row0, it.k_len, t, z, vz);
+#pragma unroll
+        for (int rgn = 0; rgn < L::NREG; ++rgn) tma_load_3d(dst + rgn * L::KV_REG, map, rgn * 64, y, z, b);
+      };
+      // Bytes one K (or V) tile brings: a whole tile, or for band items the
+      // bh x kw rows of one halo box (out-of-frame rows included).
+      const uint32_t tile_bytes = PROXY ? (uint32_t)(L::NREG * p.pg.bh * p.pg.kw * 128) : (uint32_t)L::KV_BYTES;
+      TcItem it, nx;
+      int w = next_keyed(p, w_begin, w_end, w_step, isrc, it);
+      int issued = 0;   // load groups issued (global key tile count)
+      bool k0 = false, stalled = false, fail = false;
+      if (w < w_end) {
+        mbar_expect_tx(bar(B_K0FULL), tile_bytes);
+        load_tile(sK, &args.tk, it, 0, bar(B_K0FULL));
+        k0 = true;
       }
-      if (stalled || *abort_flag || issued < n_tiles) {
+      while (w < w_end && !fail && !stalled) {
+        const int n = tc_tiles(p, it, CLS);
+        const int wn = next_keyed(p, w + w_step, w_end, w_step, isrc, nx);
+        for (int j = 0; j < n; ++j) {
+          if (p.debug_stall && issued >= 1) {
+            // Test hook: stop feeding without raising the abort flag, so that
+            // the consumers' bounded waits expire.
+            stalled = true;
+            break;
+          }
+          // Group `issued` reuses V stage issued % 2 and K stage
+          // (issued + 1) % 2, which key tile issued - 2's EMPTY commit
+          // releases (the MMA prologue's commit, counted as tile -1,
+          // releases K(0)).
+          const int st = issued % STAGES;
+          if (issued >= 1 && !mbar_wait_bounded(bar(B_EMPTY + st), ((issued - 1) / 2) & 1, abort_flag, wait_limit)) {
+            fail = true;
+            break;
+          }
+          const bool k_same = j + 1 < n, k_next = !k_same && wn < w_end;
+          mbar_expect_tx(bar(B_FULL + st), (k_same || k_next) ? 2 * tile_bytes : tile_bytes);
+          load_tile(sV + st * L::KV_BYTES, &args.tv, it, j, bar(B_FULL + st));
+          const uint32_t kdst = sK + ((issued + 1) % STAGES) * L::KV_BYTES;
+          if (k_same) load_tile(kdst, &args.tk, it, j + 1, bar(B_FULL + st));
+          else if (k_next) load_tile(kdst, &args.tk, nx, 0, bar(B_FULL + st));
+          ++issued;
+        }
+        w = wn;
+        it = nx;
+      }
+      if (stalled || fail || *abort_flag) {
         if (!stalled) *abort_flag = 1;
         // Let the copies still in flight land before the CTA's memory goes.
         volatile int zero_flag = 0;   // drains ignore the abort flag
-        (void)mbar_wait_bounded(bar(B_K0FULL), 0, &zero_flag, DRAIN_LIMIT_NS);
+        if (k0) (void)mbar_wait_bounded(bar(B_K0FULL), 0, &zero_flag, DRAIN_LIMIT_NS);
         for (int t = max(0, issued - STAGES); t < issued; ++t)
           (void)mbar_wait_bounded(bar(B_FULL + t % STAGES), (t / STAGES) & 1, &zero_flag, DRAIN_LIMIT_NS);
       }
@@ -504,7 +675,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     __syncwarp();
   } else if (warp == W_MMA) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0) {
       constexpr uint32_t ID_S = idesc_bf16(BM, BN, false);
       constexpr uint32_t ID_PV = idesc_bf16(BM, D, true);
       // Descriptors of query tile 0 and of the first K and V stage; the
@@ -516,7 +687,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       auto wait1 = [&](int slot, uint32_t parity) {
         return mbar_wait_bounded(bar(slot), parity, abort_flag, wait_limit);
       };
-      // S_i(t) = Q_i K(t)^T into S_i's TMEM columns.
+      // S_i = Q_i K(t)^T into S_i's TMEM columns (t: global key tile).
       auto mma_s = [&](int i, int t) {
         const uint64_t dk = dk0 + ((uint32_t)((t % STAGES) * L::KV_BYTES) >> 4);
         const uint64_t dq = dq0 + ((uint32_t)(i * L::Q_BYTES) >> 4);
@@ -529,42 +700,76 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         }
         if (i == 0) mma_commit(bar(B_SFULL));   // S_1: the EMPTY commit right after it
       };
-      // O_i += P_i(j) V(j), P_i from the first half of S_i's columns.
-      auto mma_pv = [&](int i, int j) {
-        const uint64_t dv = dv0 + ((uint32_t)((j % STAGES) * L::KV_BYTES) >> 4);
+      // O_i (+)= P_i V(t), P_i from the first half of S_i's columns; the
+      // item's first key tile (j == 0) starts O_i afresh.
+      // (The classification pass also starts O_i afresh at the Dummy
+      // segment's first tile.)
+      const int j_restart = CLS ? cls_n0(p) + cls_n1(p) : 0;
+      auto mma_pv = [&](int i, int t, int j) {
+        const uint64_t dv = dv0 + ((uint32_t)((t % STAGES) * L::KV_BYTES) >> 4);
+        const bool fresh = j == 0 || j == j_restart;
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks)
           mma_bf16_ts(tmem + L::COL_O + i * D, tmem + i * BN + ks * 8, dv + ((ks * 16 * 128) >> 4), ID_PV,
-                      (j > 0 || ks > 0) ? 1u : 0u);
+                      (!fresh || ks > 0) ? 1u : 0u);
       };
-      bool ok = wait1(B_K0FULL, 0);
-      if (ok) {
-        tc_fence_after();
-        mma_s(0, 0);
-        if (two) mma_s(1, 0);
-        mma_commit(bar(B_EMPTY + 1));   // tile -1: releases K(0)
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % STAGES;
-        const bool more = j + 1 < n_tiles;
-        // V(j) and K(j+1) arrive together.
-        if (!(ok = wait1(B_FULL + st, (j / STAGES) & 1))) break;
-        if (!(ok = wait1(B_PFULL + 0, j & 1))) break;
-        tc_fence_after();
-        mma_pv(0, j);
-        if (more) mma_s(0, j + 1);
-        if (two) {
-          if (!(ok = wait1(B_PFULL + 1, j & 1))) break;
+      TcItem it, nx;
+      int w = next_keyed(p, w_begin, w_end, w_step, isrc, it);
+      int gt = 0;       // global key tile
+      int qph = 0;      // QREADY phases consumed
+      bool ok = true;
+      if (w < w_end) {
+        ok = wait1(B_K0FULL, 0) && wait1(B_QREADY + 0, 0);
+        if (ok) {
           tc_fence_after();
-          mma_pv(1, j);
-          if (more) mma_s(1, j + 1);
+          mma_s(0, 0);
+          ok = wait1(B_QREADY + 1, 0);
         }
-        mma_commit(bar(B_EMPTY + st));   // releases V(j) and K(j+1)
+        if (ok) {
+          tc_fence_after();
+          mma_s(1, 0);
+          mma_commit(bar(B_EMPTY + 1));   // tile -1: releases K(0), signals S_1(0)
+        }
+        qph = 1;
       }
-      if (ok) {
-        mma_commit(bar(B_ODONE + 0));
-        if (two) mma_commit(bar(B_ODONE + 1));
-      } else {
+      while (ok && w < w_end) {
+        const int n = tc_tiles(p, it, CLS);
+        const int wn = next_keyed(p, w + w_step, w_end, w_step, isrc, nx);
+        for (int j = 0; j < n; ++j) {
+          const int st = gt % STAGES;
+          const bool last = j + 1 == n;
+          // V(gt) and K(gt+1) arrive together.
+          if (!(ok = wait1(B_FULL + st, (gt / STAGES) & 1))) break;
+          if (!(ok = wait1(B_PFULL + 0, gt & 1))) break;
+          tc_fence_after();
+          mma_pv(0, gt, j);
+          if (!last) mma_s(0, gt + 1);
+          else mma_commit(bar(B_ODONE + 0));
+          if (!(ok = wait1(B_PFULL + 1, gt & 1))) break;
+          tc_fence_after();
+          mma_pv(1, gt, j);
+          if (!last) {
+            mma_s(1, gt + 1);
+          } else {
+            mma_commit(bar(B_ODONE + 1));
+            if (wn < w_end) {
+              // The next item's first S: its query tiles, K(gt+1).
+              if (!(ok = wait1(B_QREADY + 0, qph & 1))) break;
+              tc_fence_after();
+              mma_s(0, gt + 1);
+              if (!(ok = wait1(B_QREADY + 1, qph & 1))) break;
+              tc_fence_after();
+              mma_s(1, gt + 1);
+              ++qph;
+            }
+          }
+          mma_commit(bar(B_EMPTY + st));   // releases V(gt) and K(gt+1), signals S_1(gt+1)
+          ++gt;
+        }
+        w = wn;
+        it = nx;
+      }
+      if (!ok) {
         *abort_flag = 1;
         // Every MMA issued so far must finish before TMEM is released.
         volatile int zero_flag = 0;
@@ -576,65 +781,229 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
   } else if (warp < 4 * QT) {
     // ---------------------------------------------------------------- softmax groups
     const int grp = warp >> 2, r = tid & 127, qrow = grp * BM + r;
-    const bool active = grp == 0 || two;
     const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t t_s = t_lane + grp * BN;            // S_i (and P_i over its first half)
     const uint32_t t_o = t_lane + L::COL_O + grp * D;  // O_i
     const float sl2 = g.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    int h_lo = 0, h_hi = -1, w_lo = 0, w_hi = -1;   // PROXY: this row's key window in a frame
-    if (PROXY) {
-      const int pos = (it.q0 + qrow) % g.F;
-      const int hq = pos / g.Fw;
-      band_window(g, p.band_win, hq, pos - hq * g.Fw, h_lo, h_hi, w_lo, w_hi);
-    }
+    const uint32_t q_tile = sQ + grp * L::Q_BYTES;
     auto wait_warp = [&](int slot, uint32_t parity) -> bool {
       const bool w = mbar_wait_bounded(bar(slot), parity, abort_flag, wait_limit);
       return __all_sync(0xffffffffu, w);
     };
-    for (int j = 0; active && j < n_tiles; ++j) {
-      // S_1(j) is signalled by key tile j-1's EMPTY commit (the MMA
-      // prologue's for j = 0): slot (j+1) % 2, its (j/2)-th completion.
-      const int s_slot = grp == 0 ? (int)B_SFULL : B_EMPTY + (j + 1) % STAGES;
-      if (!wait_warp(s_slot, grp == 0 ? (j & 1) : ((j / 2) & 1))) { ok = false; break; }
-      tc_fence_after();
-      const int valid = min(BN, it.k_len - j * BN);
-      const bool full = PROXY || valid == BN;   // only a key run's last tile is partial
-      // PROXY: bit e of mw[e / 32] marks key column e of this tile as inside
-      // the row's proxy window (one run of keys per window row; the band's
-      // rows are consecutive frame rows).
-      uint32_t mw[BN / 32];
+    // Row qrow of an item's query tile into the K-major 128-byte-swizzled
+    // layout (zeros past its queries) by asynchronous copies; finish_q waits
+    // for them and makes one arrival per warp on QREADY_i.
+    // Row qrow of an item's query tile into the K-major 128-byte-swizzled
+    // layout (zeros past its queries) by asynchronous copies (all 16-byte
+    // pieces of the row in flight at once); finish_q waits for them and makes
+    // one arrival per warp on QREADY_i.
+    auto issue_q = [&](const TcItem& it) {
+      const bool ok = qrow < it.nq;
+      const int tok = ok ? tc_query_token(it, g, qrow) : 0;
+      const int4* src = reinterpret_cast<const int4*>(static_cast<const bf16*>(p.q) + tok * HD + (int64_t)it.head * D);
 #pragma unroll
-      for (int w = 0; w < BN / 32; ++w) mw[w] = 0u;
-      if (PROXY) {
-        const int o = (j % it.tpf) * BN;
-        const int rhi = it.rlo + it.rlen / g.Fw - 1;
-        for (int hk = max(it.rlo, h_lo); hk <= min(rhi, h_hi); ++hk) {
-          const int a = max((hk - it.rlo) * g.Fw + w_lo - o, 0);
-          const int b = min((hk - it.rlo) * g.Fw + w_hi - o, BN - 1);
+      for (int c = 0; c < D / 8; ++c)
+        cp_async16(q_tile + (c >> 3) * L::Q_REG + r * 128 + (((c & 7) ^ (r & 7)) << 4), src + c, ok ? 16u : 0u);
+      cp_async_commit();
+    };
+    auto finish_q = [&]() {
+      cp_async_wait_all();
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QREADY + grp));
+    };
+    // Output rows of an item: the normalised output, or for a split key run
+    // the unnormalised partial with its row max and sum.
+    auto out_base = [&](const TcItem& it) -> int64_t {
+      const int64_t tok = tc_query_token(it, g, qrow);
+      return (int64_t)it.out_plane * p.o_plane_stride + tok * HD + (int64_t)it.head * D;
+    };
+    // Classification pass: park this row's running state (O as it stands in
+    // TMEM, unnormalised, with the row max and sum) in slot 0 (after the
+    // Sink segment) or 1 (before the Dummy segment).
+    auto park = [&](int w, int slot, float m, float l) {
+      const TcItem it = tc_decode(p, w, isrc);
+      const bool ok = qrow < it.nq;
+      const int64_t row = ((int64_t)slot * p.nq_total + (it.q0 + qrow)) * g.H + it.head;
 #pragma unroll
-          for (int w = 0; w < BN / 32; ++w) {
-            const int lo = max(a, 32 * w), hi = min(b, 32 * w + 31);
-            if (lo <= hi) mw[w] |= (uint32_t)(((1ull << (hi - lo + 1)) - 1ull) << (lo - 32 * w));
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_o + c * 32, o);
+        if (!ok) continue;
+        float4* dst = reinterpret_cast<float4*>(p.park_o + row * D + c * 32);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]), __uint_as_float(o[4 * e + 2]),
+                               __uint_as_float(o[4 * e + 3]));
+      }
+      if (ok) *reinterpret_cast<float2*>(p.park_ml + row * 2) = make_float2(m, l);
+    };
+    {
+      TcItem f;
+      if (next_keyed(p, w_begin, w_end, w_step, isrc, f) < w_end) {
+        issue_q(f);
+        finish_q();
+      }
+    }
+    int gt = 0;     // global key tile
+    int nitem = 0;  // keyed items done (ODONE phases)
+    bool ok = true;
+    for (int w = w_begin; ok && w < w_end; w += w_step) {
+      // Only what the tile loop needs stays live across it; the item is
+      // decoded again for the epilogue.
+      int n, k_len, rlo = 0, rlen = 0, tpf = 1;
+      int h_lo = 0, h_hi = -1, w_lo = 0, w_hi = -1;   // PROXY: this row's key window in a frame
+      {
+        const TcItem it = tc_decode(p, w, isrc);
+        n = tc_tiles(p, it, CLS);
+        k_len = it.k_len;
+        if (n == 0) {
+          // No keys: the output is defined as zero (a split run's empty
+          // share: row max -inf, sum 0).
+          if (qrow < it.nq) {
+            if (it.part >= 0) {
+              float* po = p.part_o + ((int64_t)it.part * kPartRows + qrow) * D;
+              for (int c = 0; c < D; ++c) po[c] = 0.f;
+              p.part_ml[((int64_t)it.part * kPartRows + qrow) * 2 + 0] = -INFINITY;
+              p.part_ml[((int64_t)it.part * kPartRows + qrow) * 2 + 1] = 0.f;
+            } else {
+              const int64_t base = out_base(it);
+              for (int c = 0; c < D; ++c) {
+                if (p.out_fp32) static_cast<float*>(p.o)[base + c] = 0.f;
+                else static_cast<bf16*>(p.o)[base + c] = __float2bfloat16_rn(0.f);
+              }
+            }
           }
+          continue;
+        }
+        if (PROXY) {
+          rlo = it.rlo;
+          rlen = it.rlen;
+          tpf = it.tpf;
+          const int pos = tc_query_token(it, g, qrow) % g.F;
+          const int hq = pos / g.Fw;
+          band_window(g, p.band_win, hq, pos - hq * g.Fw, h_lo, h_hi, w_lo, w_hi);
+          // As offsets into the halo (rows may start before the frame; the
+          // window is clipped to the frame, so it lies inside the halo).
+          h_lo -= rlo;
+          h_hi -= rlo;
+          w_lo -= rlen;
+          w_hi -= rlen;
         }
       }
-      // Pass 1: row max over the tile.  Without masked keys the TMEM load
-      // reduces it; otherwise 8 independent partial maxima (three-input max)
-      // over the masked values.
-      float pm[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-      if (!PROXY && full) {
-#pragma unroll
-        for (int h = 0; h < BN / 64; ++h) {
-          uint32_t x[64];
-          pm[h] = tmem_ld64_max(t_s + h * 64, x);
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < n; ++j, ++gt) {
+        // S_1(gt) is signalled by key tile gt-1's EMPTY commit (the MMA
+        // prologue's for gt = 0): slot (gt+1) % 2, its (gt/2)-th completion.
+        const int s_slot = grp == 0 ? (int)B_SFULL : B_EMPTY + (gt + 1) % STAGES;
+        if (!wait_warp(s_slot, grp == 0 ? (gt & 1) : ((gt / 2) & 1))) { ok = false; break; }
+        tc_fence_after();
+        int row_unused, valid;
+        tile_span(p, CLS, 0, k_len, j, row_unused, valid);
+        if (CLS && j > 0) {
+          // O_i holds the keys so far, complete (the commit that signalled
+          // S_i(j) covers P_i(j-1) V).
+          const int n0 = cls_n0(p), n01 = n0 + cls_n1(p);
+          if (j == n0) park(w, 0, m_run, l_run);
+          if (j == n01) {
+            park(w, 1, m_run, l_run);
+            m_run = -INFINITY;   // the Dummy segment starts afresh
+            l_run = 0.f;
+          }
         }
-      } else {
+        const bool full = PROXY || valid == BN;   // only a key run's last tile is partial
+        // PROXY: bit e of mw[e / 32] marks key column e of this tile as inside
+        // the row's proxy window (one run of keys per window row; the band's
+        // rows are consecutive frame rows).
+        uint32_t mw[BN / 32];
+#pragma unroll
+        for (int q = 0; q < BN / 32; ++q) mw[q] = 0u;
+        if (PROXY) {
+          // Key column e of box tt is halo row tt*bh + e / kw, halo column
+          // e % kw: one run of columns [w_lo, w_hi] per window row.
+          const int bh = p.pg.bh, kw = p.pg.kw;
+          const int r0 = (j % tpf) * bh;
+          for (int hk = max(r0, h_lo); hk <= min(r0 + bh - 1, h_hi); ++hk) {
+            const int a = (hk - r0) * kw + w_lo;
+            const int b = (hk - r0) * kw + w_hi;
+#pragma unroll
+            for (int q = 0; q < BN / 32; ++q) {
+              const int lo = max(a, 32 * q), hi = min(b, 32 * q + 31);
+              if (lo <= hi) mw[q] |= (uint32_t)(((1ull << (hi - lo + 1)) - 1ull) << (lo - 32 * q));
+            }
+          }
+        }
+        // Pass 1: row max over the tile.  Without masked keys the TMEM load
+        // reduces it; otherwise 8 independent partial maxima (three-input max)
+        // over the masked values.
+        float pm[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+        if (!PROXY && full) {
+#pragma unroll
+          for (int h = 0; h < BN / 64; ++h) {
+            uint32_t x[64];
+            pm[h] = tmem_ld64_max(t_s + h * 64, x);
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < BN / 64; ++h) {
+            uint32_t x[64];
+            tmem_ld32x2(t_s + h * 64, t_s + h * 64 + 32, x);
+            if (PROXY) {
+#pragma unroll
+              for (int e = 0; e < 64; ++e)
+                if (!((mw[2 * h + e / 32] >> (e & 31)) & 1u)) x[e] = __float_as_uint(-INFINITY);
+            } else if (!full) {
+#pragma unroll
+              for (int e = 0; e < 64; ++e)
+                if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              pm[u] = max3f(pm[u], __uint_as_float(x[8 * u]), __uint_as_float(x[8 * u + 1]));
+              pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 2]), __uint_as_float(x[8 * u + 3]));
+              pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 4]), __uint_as_float(x[8 * u + 5]));
+              pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 6]), __uint_as_float(x[8 * u + 7]));
+            }
+          }
+        }
+        pm[0] = max3f(pm[0], pm[1], pm[2]);
+        pm[3] = max3f(pm[3], pm[4], pm[5]);
+        pm[6] = fmaxf(pm[6], pm[7]);
+        const float m_new = fmaxf(m_run, max3f(pm[0], pm[3], pm[6]) * sl2);
+        if (j == 0 || (CLS && j == cls_n0(p) + cls_n1(p))) {
+          m_run = m_new;
+        } else if (__any_sync(0xffffffffu, m_new > m_run + RESCALE_LOG2)) {
+          // O_i holds P_i(0..j-1) V, all of it complete (the commit that
+          // signalled S_i(j) covers it): scale this warp's rows to the new max.
+          // (A row still without any unmasked key keeps m = -inf and alpha 1.)
+          const float alpha = m_new == -INFINITY ? 1.f : ex2(m_run - m_new);
+          l_run *= alpha;
+          m_run = m_new;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(t_o + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+        // Pass 2: probabilities 2^(s*scale*log2e - m), 64 keys at a time,
+        // packed two per column into P_i.  Masked keys become -inf, whose
+        // exponent is 0.
+        // A row whose keys have all been masked so far keeps m = -inf; its
+        // probabilities are all 0 (exponent of -inf), not NaN.
+        const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+        float ps[8];   // 4 independent pairs of partial sums
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ps[u] = 0.f;
 #pragma unroll
         for (int h = 0; h < BN / 64; ++h) {
+          // Keys [64h, 64h+64) of S_i; their probabilities go to P_i columns
+          // [32h, 32h+32), which lie inside S_i columns already read.
           uint32_t x[64];
           tmem_ld32x2(t_s + h * 64, t_s + h * 64 + 32, x);
           if (PROXY) {
@@ -646,120 +1015,167 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             for (int e = 0; e < 64; ++e)
               if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
           }
+          uint32_t pk[32];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u]), __uint_as_float(x[8 * u + 1]));
-            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 2]), __uint_as_float(x[8 * u + 3]));
-            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 4]), __uint_as_float(x[8 * u + 5]));
-            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 6]), __uint_as_float(x[8 * u + 7]));
+          for (int c = 0; c < 32; ++c) {
+            float a0, a1;
+            fma2(a0, a1, __uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1]), sl2, neg_m);
+            const float e0 = ex2(a0), e1 = ex2(a1);
+            add2(ps[2 * (c & 3)], ps[2 * (c & 3) + 1], e0, e1);
+            pk[c] = pack_bf16(e0, e1);
           }
+          tmem_st32(t_s + h * 32, pk);
+        }
+        l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PFULL + grp));
+      }
+      if (!ok) break;
+      {
+        // S_i of the item's last tile has been consumed: the query tile is
+        // free for the next item, whose rows load in one round trip.
+        TcItem nx;
+        if (next_keyed(p, w + w_step, w_end, w_step, isrc, nx) < w_end) {
+          issue_q(nx);
+          finish_q();
         }
       }
-      pm[0] = max3f(pm[0], pm[1], pm[2]);
-      pm[3] = max3f(pm[3], pm[4], pm[5]);
-      pm[6] = fmaxf(pm[6], pm[7]);
-      const float m_new = fmaxf(m_run, max3f(pm[0], pm[3], pm[6]) * sl2);
-      if (j == 0) {
-        m_run = m_new;
-      } else if (__any_sync(0xffffffffu, m_new > m_run + RESCALE_LOG2)) {
-        // O_i holds P_i(0..j-1) V, all of it complete (the commit that
-        // signalled S_i(j) covers it): scale this warp's rows to the new max.
-        // (A row still without any unmasked key keeps m = -inf and alpha 1.)
-        const float alpha = m_new == -INFINITY ? 1.f : ex2(m_run - m_new);
-        l_run *= alpha;
-        m_run = m_new;
+      // ---------------------------------------------------------------- epilogue
+      if (!wait_warp(B_ODONE + grp, nitem & 1)) { ok = false; break; }
+      ++nitem;
+      tc_fence_after();
+      const TcItem it = tc_decode(p, w, isrc);
+      // Final outputs are normalised; a split run's partial keeps O
+      // unnormalised, with its row max and sum.
+      const int mine_ok = qrow < it.nq ? 1 : 0;
+      if (CLS) {
+        // The Dummy segment's state is in TMEM; the Sink state and the state
+        // before the Dummy segment are parked.  Full output = the two merged
+        // (the softmax over all keys); then this token's cosines of the full
+        // output with the Sink, Dummy and proxy outputs and the proxy's
+        // squared error.
+        const int token = it.q0 + qrow;
+        const int64_t row = (int64_t)token * g.H + it.head;
+        const int64_t row1 = ((int64_t)p.nq_total + token) * g.H + it.head;
+        float2 ma = make_float2(0.f, 1.f), mb = make_float2(-INFINITY, 0.f);
+        if (mine_ok) {
+          ma = *reinterpret_cast<const float2*>(p.park_ml + row * 2);
+          mb = *reinterpret_cast<const float2*>(p.park_ml + row1 * 2);
+        }
+        const float M = fmaxf(mb.x, m_run);
+        const float fb = mb.x == -INFINITY ? 0.f : ex2(mb.x - M), fd = ex2(m_run - M);
+        const float Lf = mb.y * fb + l_run * fd;
+        const float inv_f = Lf > 0.f ? 1.f / Lf : 0.f, inv_a = ma.y > 0.f ? 1.f / ma.y : 0.f;
+        const float inv_d = l_run > 0.f ? 1.f / l_run : 0.f;
+        const float cb = fb * inv_f, cd = fd * inv_f;
+        float ff = 0.f, ss = 0.f, dd = 0.f, pp = 0.f, fs = 0.f, fdm = 0.f, fq = 0.f, se = 0.f;
+        const float* pa = p.park_o + row * D;
+        const float* pb = p.park_o + row1 * D;
+        const float* pq = p.proxy_o + row * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(t_o + c * 32, o);
-  #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(t_o + c * 32, o);
+          if (!mine_ok) continue;
+          uint32_t packed[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(pa + c * 32 + 4 * e4);
+            const float4 b4 = *reinterpret_cast<const float4*>(pb + c * 32 + 4 * e4);
+            const float4 q4 = *reinterpret_cast<const float4*>(pq + c * 32 + 4 * e4);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+            const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+            float fv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float dv = __uint_as_float(o[4 * e4 + u]);
+              const float f = bv[u] * cb + dv * cd;     // full
+              const float sk = av[u] * inv_a;           // Sink
+              const float dm = dv * inv_d;              // Dummy
+              const float pr = qv[u];                   // proxy
+              fv[u] = f;
+              ff = fmaf(f, f, ff);
+              ss = fmaf(sk, sk, ss);
+              dd = fmaf(dm, dm, dd);
+              pp = fmaf(pr, pr, pp);
+              fs = fmaf(f, sk, fs);
+              fdm = fmaf(f, dm, fdm);
+              fq = fmaf(f, pr, fq);
+              se = fmaf(pr - f, pr - f, se);
+            }
+            packed[2 * e4] = pack_bf16(fv[0], fv[1]);
+            packed[2 * e4 + 1] = pack_bf16(fv[2], fv[3]);
+            if (p.o_full && p.out_fp32)
+              reinterpret_cast<float4*>(static_cast<float*>(p.o_full) + row * D + c * 32)[e4] =
+                  make_float4(fv[0], fv[1], fv[2], fv[3]);
+          }
+          if (p.o_full && !p.out_fp32) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(p.o_full) + row * D + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+          }
         }
-        tmem_wait_st();
-      }
-      // Pass 2: probabilities 2^(s*scale*log2e - m), 64 keys at a time,
-      // packed two per column into P_i.  Masked keys become -inf, whose
-      // exponent is 0.
-      // A row whose keys have all been masked so far keeps m = -inf; its
-      // probabilities are all 0 (exponent of -inf), not NaN.
-      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-      float ps[8];   // 4 independent pairs of partial sums
-#pragma unroll
-      for (int u = 0; u < 8; ++u) ps[u] = 0.f;
-#pragma unroll
-      for (int h = 0; h < BN / 64; ++h) {
-        // Keys [64h, 64h+64) of S_i; their probabilities go to P_i columns
-        // [32h, 32h+32), which lie inside S_i columns already read.
-        uint32_t x[64];
-        tmem_ld32x2(t_s + h * 64, t_s + h * 64 + 32, x);
-        if (PROXY) {
-#pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (!((mw[2 * h + e / 32] >> (e & 31)) & 1u)) x[e] = __float_as_uint(-INFINITY);
-        } else if (!full) {
-#pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
+        if (mine_ok) {
+          // Cosine with cos(0, 0) = 1 and cos(x, 0) = 0.
+          auto cosine = [](float dot, float na2, float nb2) {
+            if (na2 == 0.f && nb2 == 0.f) return 1.f;
+            if (na2 == 0.f || nb2 == 0.f) return 0.f;
+            return dot / (sqrtf(na2) * sqrtf(nb2));
+          };
+          const int64_t n = p.nq_total;
+          p.tok[(0 * (int64_t)g.H + it.head) * n + token] = cosine(fs, ff, ss);
+          p.tok[(1 * (int64_t)g.H + it.head) * n + token] = cosine(fdm, ff, dd);
+          p.tok[(2 * (int64_t)g.H + it.head) * n + token] = cosine(fq, ff, pp);
+          p.tok[(3 * (int64_t)g.H + it.head) * n + token] = se;
         }
-        uint32_t pk[32];
+      } else if (it.part >= 0) {
+        float* po = p.part_o + ((int64_t)it.part * kPartRows + qrow) * D;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float a0, a1;
-          fma2(a0, a1, __uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1]), sl2, neg_m);
-          const float e0 = ex2(a0), e1 = ex2(a1);
-          add2(ps[2 * (c & 3)], ps[2 * (c & 3) + 1], e0, e1);
-          pk[c] = pack_bf16(e0, e1);
-        }
-        tmem_st32(t_s + h * 32, pk);
-      }
-      l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL + grp));
-    }
-    // ---------------------------------------------------------------- epilogue
-    if (active && ok && n_tiles > 0 && wait_warp(B_ODONE + grp, 0)) {
-      tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const bool w = qrow < it.nq;
-      const int64_t tok = w ? tc_query_token(it, g, qrow) : 0;
-      const int64_t base = (int64_t)it.out_plane * p.o_plane_stride + tok * HD + (int64_t)it.head * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(t_o + c * 32, o);
-        if (!w) continue;
-        if (p.out_fp32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + base + c * 32);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c * 32, o);
+          if (!mine_ok) continue;
+          float4* dst = reinterpret_cast<float4*>(po + c * 32);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
-                                 __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(p.o) + base + c * 32);
+            dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                 __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+        }
+      } else {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const int64_t base = mine_ok ? out_base(it) : 0;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t* x = o + 8 * e;
-            dst[e] = make_uint4(pack_bf16(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
-                                pack_bf16(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
-                                pack_bf16(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
-                                pack_bf16(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c * 32, o);
+          if (!mine_ok) continue;
+          if (p.out_fp32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + base + c * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                   __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(p.o) + base + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t* x = o + 8 * e;
+              dst[e] = make_uint4(pack_bf16(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                                  pack_bf16(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                                  pack_bf16(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                                  pack_bf16(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+            }
           }
         }
       }
-    } else if (active && n_tiles == 0 && qrow < it.nq) {
-      // No keys: the output is defined as zero.
-      const int64_t tok = tc_query_token(it, g, qrow);
-      const int64_t base = (int64_t)it.out_plane * p.o_plane_stride + tok * HD + (int64_t)it.head * D;
-      for (int c = 0; c < D; ++c) {
-        if (p.out_fp32) static_cast<float*>(p.o)[base + c] = 0.f;
-        else static_cast<bf16*>(p.o)[base + c] = __float2bfloat16_rn(0.f);
-      }
-    } else if (active && n_tiles > 0) {
-      *abort_flag = 1;
+      if (it.part >= 0 && mine_ok)
+        *reinterpret_cast<float2*>(p.part_ml + ((int64_t)it.part * kPartRows + qrow) * 2) = make_float2(m_run, l_run);
+      tc_fence_before();   // the next item's first P_i V overwrites O_i after the next PFULL
     }
+    if (!ok) *abort_flag = 1;
   }
 
   tc_fence_before();
@@ -768,6 +1184,45 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
   if (warp == W_MMA) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- split-run merge
+//
+// One warp per query row of a split item: the partials of its chunks, each
+// O_c = sum_j 2^(s_j - m_c) v_j with row sum l_c over the chunk's keys, merge
+// into O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c with M = max_c m_c,
+// the softmax over the union of the chunks' keys.
+
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const CombineParams c) {
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int s = gw / kPartRows, r = gw - s * kPartRows;
+  if (s >= c.n_items) return;
+  const SplitItem si = c.items[s];
+  if (r >= si.nq) return;
+  float M = -INFINITY;
+  for (int k = 0; k < si.n_chunks; ++k) M = fmaxf(M, c.part_ml[((int64_t)(si.part0 + k) * kPartRows + r) * 2]);
+  float acc[D / 32];
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  for (int k = 0; k < si.n_chunks; ++k) {
+    const int64_t row = (int64_t)(si.part0 + k) * kPartRows + r;
+    const float m = c.part_ml[row * 2], l = c.part_ml[row * 2 + 1];
+    if (m == -INFINITY) continue;   // an empty share
+    const float f = exp2f(m - M);
+    L = fmaf(l, f, L);
+    const float* po = c.part_o + row * D;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) acc[e] = fmaf(po[lane + 32 * e], f, acc[e]);
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int64_t base = ((int64_t)(si.q0 + r) * c.g.H + si.head) * D;
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) {
+    if (c.out_fp32) static_cast<float*>(c.o)[base + lane + 32 * e] = acc[e] * inv;
+    else static_cast<bf16*>(c.o)[base + lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
   }
 }
 
@@ -791,6 +1246,24 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// K or V of band launches as a 5-D bf16 tensor [frames][Fh][Fw][heads][d];
+// box {64, 1, kw, bh, 1} (one key box of a patch's halo), 128-byte swizzle.
+cudaError_t make_band_map(CUtensorMap* m, const void* base, const Geom& g, int heads, int64_t frames, int kw,
+                          int bh) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t e = 2;
+  const cuuint64_t dims[5] = {(cuuint64_t)g.d, (cuuint64_t)heads, (cuuint64_t)g.Fw, (cuuint64_t)g.Fh, (cuuint64_t)frames};
+  const cuuint64_t strides[4] = {(cuuint64_t)g.d * e, (cuuint64_t)heads * g.d * e, (cuuint64_t)g.Fw * heads * g.d * e,
+                                 (cuuint64_t)g.F * heads * g.d * e};
+  const cuuint32_t box[5] = {64, 1, (cuuint32_t)kw, (cuuint32_t)bh, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // K or V as a 3-D bf16 tensor [rows][heads][d]; box {64, 1, BN}, 128-byte swizzle.
 cudaError_t make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows) {
   EncodeTiledFn enc = encode_fn();
@@ -805,9 +1278,17 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, bool PROXY>
-cudaError_t launch_d(const TcArgs& a, dim3 grid, cudaStream_t s) {
-  constexpr int smem = Layout<D>::ALLOC;
+// Dynamic shared memory of a launch: the layout's bytes, but never less than
+// half of an SM's shared memory, so that one CTA runs per SM (a second one
+// would wait on its TMEM allocation while holding shared memory).
+template <int D>
+constexpr int smem_request() {
+  return Layout<D>::ALLOC > 118 * 1024 ? Layout<D>::ALLOC : 118 * 1024;
+}
+
+template <int D, bool PROXY, bool CLS>
+cudaError_t launch_d(const TcArgs& a, int ctas, cudaStream_t s) {
+  constexpr int smem = smem_request<D>();
   static_assert(smem <= 232448, "shared memory budget");
   // The dynamic shared-memory opt-in is a per-device attribute of the
   // function: set it once on every device the process launches on.
@@ -821,12 +1302,12 @@ cudaError_t launch_d(const TcArgs& a, dim3 grid, cudaStream_t s) {
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!configured[dev]) {
-      e = cudaFuncSetAttribute(attn_tc_kernel<D, PROXY>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      e = cudaFuncSetAttribute(attn_tc_kernel<D, PROXY, CLS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       configured[dev] = true;
     }
   }
-  attn_tc_kernel<D, PROXY><<<grid, NTHREADS, smem, s>>>(a);
+  attn_tc_kernel<D, PROXY, CLS><<<ctas, NTHREADS, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -834,24 +1315,60 @@ cudaError_t launch_d(const TcArgs& a, dim3 grid, cudaStream_t s) {
 
 int tc_block_rows() { return QT * BM; }
 
-cudaError_t launch_attention_tc(const AttnParams& p, const TcKV& kv, dim3 grid, cudaStream_t s) {
-  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
+int device_sm_count() {
+  constexpr int kMaxDevices = 128;
+  static std::mutex mu;
+  static int count[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kPlanCtas;
+  std::lock_guard<std::mutex> lock(mu);
+  if (count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kPlanCtas;
+    count[dev] = n;
+  }
+  return count[dev];
+}
+
+cudaError_t launch_attention_tc(const AttnParams& p, const TcKV& kv, int ctas, cudaStream_t s) {
+  if (ctas <= 0 || p.n_items <= 0) return cudaSuccess;
   if (p.g.d != 64 && p.g.d != 128) return cudaErrorInvalidValue;
   if (kv.rows <= 0 || kv.rows > 0x7fffffffll) return cudaErrorInvalidValue;
   TcArgs a;
   memset(&a, 0, sizeof a);
-  cudaError_t e = make_map(&a.tk, kv.k, p.g.d, kv.heads, kv.rows);
-  if (e != cudaSuccess) return e;
-  if ((e = make_map(&a.tv, kv.v, p.g.d, kv.heads, kv.rows)) != cudaSuccess) return e;
+  const bool band = p.item_mode == ITEMS_PROXY || p.band_win == WIN_SLIDING;
+  cudaError_t e;
+  if (band) {
+    // Band launches read boxes of a patch's halo: K and V as frames of
+    // Fh x Fw tokens (every key run of the cache is whole frames).
+    if (kv.rows % p.g.F != 0 || p.pg.kw < 1 || p.pg.kw > 128 || p.pg.bh < 1 || p.pg.bh * p.pg.kw > BN)
+      return cudaErrorInvalidValue;
+    const int64_t frames = kv.rows / p.g.F;
+    if ((e = make_band_map(&a.tk, kv.k, p.g, kv.heads, frames, p.pg.kw, p.pg.bh)) != cudaSuccess) return e;
+    if ((e = make_band_map(&a.tv, kv.v, p.g, kv.heads, frames, p.pg.kw, p.pg.bh)) != cudaSuccess) return e;
+  } else {
+    if ((e = make_map(&a.tk, kv.k, p.g.d, kv.heads, kv.rows)) != cudaSuccess) return e;
+    if ((e = make_map(&a.tv, kv.v, p.g.d, kv.heads, kv.rows)) != cudaSuccess) return e;
+  }
   a.p = p;
   a.p.debug_stall = debug_stall_enabled() ? 1 : 0;
   a.p.wait_limit_ns = a.p.debug_stall ? STALL_WAIT_LIMIT_NS : WAIT_LIMIT_NS;
   a.kv_head_coord = kv.heads > 1 ? 1 : 0;
   // Band items (classification proxy, routed sliding Spatial) run the masked
   // variant; the caller launches them separately from the other items.
-  if (p.item_mode == ITEMS_PROXY || p.band_win == WIN_SLIDING)
-    return p.g.d == 128 ? launch_d<128, true>(a, grid, s) : launch_d<64, true>(a, grid, s);
-  return p.g.d == 128 ? launch_d<128, false>(a, grid, s) : launch_d<64, false>(a, grid, s);
+  if (band) return p.g.d == 128 ? launch_d<128, true, false>(a, ctas, s) : launch_d<64, true, false>(a, ctas, s);
+  if (p.cls) return p.g.d == 128 ? launch_d<128, false, true>(a, ctas, s) : launch_d<64, false, true>(a, ctas, s);
+  return p.g.d == 128 ? launch_d<128, false, false>(a, ctas, s) : launch_d<64, false, false>(a, ctas, s);
+}
+
+cudaError_t launch_combine(const CombineParams& c, cudaStream_t s) {
+  if (c.n_items <= 0) return cudaSuccess;
+  const int64_t threads = (int64_t)c.n_items * kPartRows * 32;
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (c.g.d == 128) combine_kernel<128><<<blocks, 256, 0, s>>>(c);
+  else if (c.g.d == 64) combine_kernel<64><<<blocks, 256, 0, s>>>(c);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 }  // namespace hc

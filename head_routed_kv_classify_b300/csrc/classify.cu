@@ -30,11 +30,17 @@ __device__ __forceinline__ float cosine(float dot, float na2, float nb2) {
   return dot / (sqrtf(na2) * sqrtf(nb2));
 }
 
+// A set status word means an attention launch of this classification gave
+// up on a bounded wait: its output planes are incomplete.
+__device__ __forceinline__ bool planes_incomplete(const ClassifyPost& c) {
+  return c.status && *reinterpret_cast<const volatile int*>(c.status) != DEV_OK;
+}
+
 // One warp per (token, head) row.
 __global__ void cos_kernel(const ClassifyPost c) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int H = c.g.H, d = c.g.d;
-  if (gw >= c.nq * H) return;
+  if (gw >= c.nq * H || planes_incomplete(c)) return;
   const int i = gw / H, h = gw - i * H;
   const int64_t row = ((int64_t)i * H + h) * d;
   const float* pf = c.planes + row;
@@ -132,7 +138,17 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const ClassifyPost 
   __shared__ uint32_t hist[256];
   __shared__ int sh[2];
   __shared__ double red[33];
+  __shared__ int incomplete;
   const int h = blockIdx.x, H = c.g.H, n = c.nq;
+  // Read once and shared, so that the whole block takes the same branch.
+  if (threadIdx.x == 0) incomplete = planes_incomplete(c) ? 1 : 0;
+  __syncthreads();
+  if (incomplete) {
+    // No label can be decided: mark the head with an invalid label (-1),
+    // which the cache calls reject.
+    if (threadIdx.x == 0) c.labels[h] = -1;
+    return;
+  }
   const float* cs = c.tok + (0 * (int64_t)H + h) * n;
   const float* cd = c.tok + (1 * (int64_t)H + h) * n;
   const float* cp = c.tok + (2 * (int64_t)H + h) * n;
@@ -184,9 +200,11 @@ cudaError_t launch_classify_post(const ClassifyPost& c, cudaStream_t s) {
   const int64_t rows = (int64_t)c.nq * c.g.H;
   const int threads = 256;
   const int64_t blocks = (rows * 32 + threads - 1) / threads;
-  cos_kernel<<<(unsigned)blocks, threads, 0, s>>>(c);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (!c.tokens_ready) {
+    cos_kernel<<<(unsigned)blocks, threads, 0, s>>>(c);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   reduce_kernel<<<c.g.H, kRedThreads, 0, s>>>(c);
   return cudaGetLastError();
 }

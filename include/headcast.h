@@ -39,6 +39,11 @@
  *    calling thread.
  *  - Thread safety.  Distinct handles may be used from distinct threads.  A
  *    handle must not be used on two streams at once.
+ *  - Devices.  The library keeps a few per-device facts once it has seen a
+ *    device (the addresses of its device-side status word and static
+ *    workspace, kernel attributes, the SM count).  cudaDeviceReset, or any
+ *    other way of replacing a device's primary context, while the library is
+ *    in use is not supported: those cached addresses would then be stale.
  */
 #ifndef HEADCAST_H
 #define HEADCAST_H
@@ -50,7 +55,7 @@
 extern "C" {
 #endif
 
-#define HC_ABI_VERSION 3
+#define HC_ABI_VERSION 4
 #define HC_MAX_HEADS 64
 
 typedef enum { HC_SINK = 0, HC_DUMMY = 1, HC_SPATIAL = 2, HC_GLOBAL = 3 } hc_archetype;
@@ -121,6 +126,9 @@ typedef struct {
   int32_t n_by_archetype[4];/* heads per archetype                            */
   int64_t rows_by_archetype[4]; /* K rows reserved per archetype (V the same) */
   size_t bytes;             /* bytes of the backing store actually used       */
+  size_t kv_bytes;          /* of which the per-archetype K and V regions     */
+  size_t split_bytes;       /* of which the routed launch's workspace for key
+                               runs split across CTAs (0 if none is split)    */
   size_t monolithic_bytes;  /* bytes a [window][H][d] K+V cache would take    */
 } hc_cache_info;
 
@@ -170,6 +178,10 @@ hc_status hc_config_validate(const hc_config* cfg);
  * scratch       device workspace of at least hc_classify_scratch_bytes(),
  *               16-byte aligned, owned by the caller, contents undefined
  *               after the call.
+ * If a bounded device-side wait expires in one of the call's kernels (or the
+ * status word was already set when they ran), no label is decided:
+ * labels_dev holds -1 for every head, and with labels_host the call returns
+ * HC_ERR_TIMEOUT (the status word stays set for hc_get_last_error).
  * ------------------------------------------------------------------------- */
 hc_status hc_classify_scratch_bytes(const hc_config* cfg, int32_t n_key_frames, size_t* bytes);
 hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const void* v,
@@ -232,6 +244,11 @@ hc_status hc_cache_create(const hc_config* cfg, const int8_t* labels_host, void*
                           size_t bytes, hc_cache** out);
 hc_status hc_cache_destroy(hc_cache* cache);
 hc_status hc_cache_get_info(const hc_cache* cache, hc_cache_info* out);
+/* The same summary for a cache not yet created (HOST only, no device
+ * access): what hc_cache_create would reserve for these labels.  The
+ * steady-state memory comparison of the restructured cache with the
+ * monolithic one [Pith review, Figure 9 caption / Appendix C]. */
+hc_status hc_cache_plan_info(const hc_config* cfg, const int8_t* labels_host, hc_cache_info* out);
 
 /* Fill the per-archetype regions from a monolithic window.
  * k_win, v_win  [n_blocks*3F][H][d] holding blocks first_block_id ..
@@ -257,7 +274,10 @@ hc_status hc_cache_append(hc_cache* cache, int64_t block_id, const void* k_blk,
  * softmax(q k^T * scale) v over: Sink -> block 0; Dummy -> newest block;
  * Spatial -> the query's cell in every filled ring slot (HC_SPATIAL_SLIDING:
  * the window centred on the query); Global -> every filled ring slot.  No
- * mask inside a block.  Async (one launch; two with sliding Spatial heads).
+ * mask inside a block.  Async: one persistent launch over all heads and
+ * pathways (plus one for sliding Spatial heads, and a light merge launch
+ * when the plan splits long key runs across CTAs).  A handle's launches
+ * share its split workspace, so one handle's calls must not overlap.
  * [Pith review, "The pith", "Core claim", Figure 3 caption.]
  * ------------------------------------------------------------------------- */
 hc_status hc_routed_attention(const hc_cache* cache, const void* q, void* o, void* stream);

@@ -47,7 +47,7 @@ def test_library_does_not_need_libcuda(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.hc_abi_version() == hc.ABI_VERSION == 3
+    assert lib.hc_abi_version() == hc.ABI_VERSION == 4
     assert lib.hc_status_string(0) == b"ok"
     assert lib.hc_status_string(7) == b"device-side wait expired"
 
@@ -84,12 +84,36 @@ def test_cache_bytes_720p(lib):
     cfg = hc.make_config(12, 128, 45, 80)
     labels = [0, 0, 1, 1, 1, 2, 2, 2, 2, 3, 3, 3]
     n = hc.hc_cache_bytes(cfg, labels)
+    info = hc.hc_cache_plan_info(cfg, labels)
     F, d = 3600, 128
     rows = 5 * 3 * F + 7 * 21 * F
-    assert n >= 2 * rows * d * 2
-    assert n < 2 * rows * d * 2 + 2 * 1024 * 1024      # work list + alignment
+    assert info["bytes"] == n and info["kv_bytes"] == 2 * rows * d * 2
+    assert info["rows_by_archetype"] == [2 * 3 * F, 3 * 3 * F, 4 * 21 * F, 3 * 21 * F]
+    assert info["n_by_archetype"] == [2, 3, 4, 3] and info["newest_block"] == -1
+    # work list, schedule and alignment on top of the K/V regions and the split workspace
+    assert info["kv_bytes"] + info["split_bytes"] <= n < info["kv_bytes"] + info["split_bytes"] + 2 * 1024 * 1024
     mono = 2 * 21 * F * 12 * d * 2
-    assert n < 0.66 * mono
+    assert info["monolithic_bytes"] == mono and n < 0.66 * mono
+
+
+@pytest.mark.parametrize("name,split", [("480p", True), ("720p", False), ("1080p", False)])
+def test_long_key_runs_are_split_only_where_they_outlast_the_launch(lib, name, split):
+    """The planner splits a Global head's key run across CTAs when one
+    256-query item over the whole window is longer than an even share of the
+    launch over 148 SMs (the 480P layer: 256 key tiles against about 136),
+    and leaves the larger layers, whose items are shorter than that share,
+    unsplit.  Split runs need a workspace of 256 rows x d fp32 per piece."""
+    import synth
+    shape = synth.SHAPES[name]
+    info = hc.hc_cache_plan_info(hc.config_for(shape), shape.mix)
+    if split:
+        per_piece = 256 * (shape.head_dim + 2) * 4
+        assert info["split_bytes"] >= 2 * 3 * per_piece       # >= 2 pieces per Global item
+    else:
+        assert info["split_bytes"] == 0
+    cfg32 = hc.config_for(shape)
+    cfg32.dtype = hc.HC_FP32                                  # the fp32 path never splits
+    assert hc.hc_cache_plan_info(cfg32, shape.mix)["split_bytes"] == 0
 
 
 def test_cache_bytes_rejects_bad_labels(lib):

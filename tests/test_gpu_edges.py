@@ -2,7 +2,8 @@
 cache still in warm-up (window not full yet, so Global and Spatial heads see
 fewer frames and the Sink block is also the newest), the maximum head count,
 a proxy radius of 0 (each query's own position), a cell covering one axis
-only, and a single-head d = 64 layer."""
+only, a single-head d = 64 layer, and key runs split across CTAs whose
+pieces are empty while the window fills."""
 import numpy as np
 import pytest
 
@@ -117,4 +118,28 @@ def test_cell_covering_one_axis_and_single_head():
     cache.restructure(gu.to_dev(inp.k, "bf16"), gu.to_dev(inp.v, "bf16"), 0)
     o = gu.to_host(cache.routed_attention(gu.to_dev(inp.q, "bf16")))
     gu.assert_close(o, ref.routed_attention(inp.q.values, cache_ref, [2]), "bf16", "one-axis cell")
+    hc.hc_get_last_error()
+
+
+def test_split_key_runs_with_empty_pieces_during_warm_up():
+    """One-frame blocks and a 16-frame window: a Global head's run of 16 x 480
+    keys (60 tiles) is split into 8 pieces, so with one frame in the window
+    (4 tiles) half of the pieces hold no key and must merge as empty shares.
+    Checked against the oracle while the window fills and after it wraps."""
+    shape = synth.LayerShape("split", 2, 64, 24, 20, 16, "bf16", 36, (3, 1), frames_per_block=1)
+    cfg = hc.config_for(shape)
+    info = hc.hc_cache_plan_info(cfg, [3, 1])
+    assert info["split_bytes"] >= 2 * 8 * 256 * 66 * 4      # 2 items x 8 pieces
+    geom = ref.geometry_of(shape)
+    cache_ref = ref.CacheModel(geom)
+    cache = hc.hc_cache_create(cfg, [3, 1])
+    labels = [3, 1]
+    for b in range(18):
+        q, k, v = synth.make_block(shape, seed=700 + b)
+        cache.append(b, gu.to_dev(k, "bf16"), gu.to_dev(v, "bf16"))
+        cache_ref.put(b, k.values, v.values)
+        if b in (0, 1, 5, 15, 17):
+            o = gu.to_host(cache.routed_attention(gu.to_dev(q, "bf16")))
+            want = ref.routed_attention(q.values, cache_ref, labels)
+            gu.assert_close(o, want, "bf16", f"split runs after block {b}")
     hc.hc_get_last_error()
