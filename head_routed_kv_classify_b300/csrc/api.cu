@@ -568,6 +568,16 @@ hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const 
     pc.cls = 1;
     pc.seg_sink = g.blk;
     pc.seg_dummy = (int32_t)(nk - g.blk);
+    {
+      const int kt = hc::tc_key_tile();
+      const int n0 = (pc.seg_sink + kt - 1) / kt, n1 = (pc.seg_dummy - pc.seg_sink + kt - 1) / kt;
+      const int n2 = ((int)nk - pc.seg_dummy + kt - 1) / kt;
+      pc.cls_n0 = n0;
+      pc.cls_n01 = n0 + n1;
+      pc.cls_v0 = pc.seg_sink - (n0 - 1) * kt;
+      pc.cls_v1 = n1 > 0 ? (pc.seg_dummy - pc.seg_sink) - (n1 - 1) * kt : 0;
+      pc.cls_v2 = ((int)nk - pc.seg_dummy) - (n2 - 1) * kt;
+    }
     pc.park_o = reinterpret_cast<float*>(sc + CL.off_park);
     pc.park_ml = reinterpret_cast<float*>(sc + CL.off_park_ml);
     pc.proxy_o = reinterpret_cast<const float*>(sc + CL.off_proxy);

@@ -420,42 +420,32 @@ __device__ __forceinline__ TcItem tc_decode(const AttnParams& p, int w, const Wo
   return it;
 }
 
-// Classification full pass: key tiles of the Sink and middle segments (the
-// Dummy segment's follow).
-__device__ __forceinline__ int cls_n0(const AttnParams& p) { return (p.seg_sink + BN - 1) / BN; }
-__device__ __forceinline__ int cls_n1(const AttnParams& p) { return (p.seg_dummy - p.seg_sink + BN - 1) / BN; }
-
+// Classification full pass: the key tiles run as Sink segment [0, cls_n0),
+// middle [cls_n0, cls_n01) and Dummy segment [cls_n01, n), each ending in
+// its own partial tile.  The boundaries are launch constants, so a tile
+// needs a few compares against parameters and no live registers (this code
+// runs on the critical path of every key tile).
 __device__ __forceinline__ int tc_tiles(const AttnParams& p, const TcItem& it, bool cls) {
   if (it.k_len <= 0) return 0;
-  if (cls) return cls_n0(p) + cls_n1(p) + (it.k_len - p.seg_dummy + BN - 1) / BN;
+  if (cls) return p.cls_n01 + (it.k_len - p.seg_dummy + BN - 1) / BN;
   return (it.k_len + BN - 1) / BN;
 }
 
-// First key row and valid keys of key tile j (segments of the
-// classification pass each end in their own partial tile).
-__device__ __forceinline__ void tile_span(const AttnParams& p, bool cls, int64_t k_row0, int k_len, int j, int& row,
-                                          int& valid) {
-  if (cls) {
-    const int n0 = cls_n0(p), n1 = cls_n1(p);
-    int a, b;
-    if (j < n0) {
-      a = 0;
-      b = p.seg_sink;
-    } else if (j < n0 + n1) {
-      a = p.seg_sink;
-      b = p.seg_dummy;
-      j -= n0;
-    } else {
-      a = p.seg_dummy;
-      b = k_len;
-      j -= n0 + n1;
-    }
-    row = (int)k_row0 + a + j * BN;
-    valid = min(BN, b - a - j * BN);
-    return;
-  }
-  row = (int)k_row0 + j * BN;
-  valid = min(BN, k_len - j * BN);
+// First key row of key tile j.
+__device__ __forceinline__ int tile_row(const AttnParams& p, bool cls, int64_t k_row0, int j) {
+  if (!cls) return (int)k_row0 + j * BN;
+  const int seg0 = j < p.cls_n0 ? 0 : (j < p.cls_n01 ? p.seg_sink - p.cls_n0 * BN : p.seg_dummy - p.cls_n01 * BN);
+  return (int)k_row0 + seg0 + j * BN;
+}
+
+// Keys in key tile j of n.
+__device__ __forceinline__ int tile_valid(const AttnParams& p, bool cls, int k_len, int j, int n) {
+  if (!cls) return min(BN, k_len - j * BN);
+  int v = BN;
+  v = j == p.cls_n0 - 1 ? p.cls_v0 : v;
+  v = j == p.cls_n01 - 1 && p.cls_n01 > p.cls_n0 ? p.cls_v1 : v;
+  v = j == n - 1 ? p.cls_v2 : v;
+  return v;
 }
 
 // The items of this CTA: w0, w0 + step, ... below w1.
@@ -616,8 +606,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             tma_load_5d(dst + rgn * L::KV_REG, map, rgn * 64, y, it.rlen, it.rlo + tt * p.pg.bh, fr, b);
           return;
         }
-        int z, vz;
-        tile_span(p, CLS, it.k_row0, it.k_len, t, z, vz);
+        const int z = tile_row(p, CLS, it.k_row0, t);
 #pragma unroll
         for (int rgn = 0; rgn < L::NREG; ++rgn) tma_load_3d(dst + rgn * L::KV_REG, map, rgn * 64, y, z, b);
       };
@@ -704,7 +693,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       // item's first key tile (j == 0) starts O_i afresh.
       // (The classification pass also starts O_i afresh at the Dummy
       // segment's first tile.)
-      const int j_restart = CLS ? cls_n0(p) + cls_n1(p) : 0;
+      const int j_restart = CLS ? p.cls_n01 : 0;
       auto mma_pv = [&](int i, int t, int j) {
         const uint64_t dv = dv0 + ((uint32_t)((t % STAGES) * L::KV_BYTES) >> 4);
         const bool fresh = j == 0 || j == j_restart;
@@ -898,12 +887,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         const int s_slot = grp == 0 ? (int)B_SFULL : B_EMPTY + (gt + 1) % STAGES;
         if (!wait_warp(s_slot, grp == 0 ? (gt & 1) : ((gt / 2) & 1))) { ok = false; break; }
         tc_fence_after();
-        int row_unused, valid;
-        tile_span(p, CLS, 0, k_len, j, row_unused, valid);
-        if (CLS && j > 0) {
+        const int valid = tile_valid(p, CLS, k_len, j, n);
+        if (CLS && (j == p.cls_n0 || j == p.cls_n01)) {
           // O_i holds the keys so far, complete (the commit that signalled
           // S_i(j) covers P_i(j-1) V).
-          const int n0 = cls_n0(p), n01 = n0 + cls_n1(p);
+          const int n0 = p.cls_n0, n01 = p.cls_n01;
           if (j == n0) park(w, 0, m_run, l_run);
           if (j == n01) {
             park(w, 1, m_run, l_run);
@@ -972,7 +960,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         pm[3] = max3f(pm[3], pm[4], pm[5]);
         pm[6] = fmaxf(pm[6], pm[7]);
         const float m_new = fmaxf(m_run, max3f(pm[0], pm[3], pm[6]) * sl2);
-        if (j == 0 || (CLS && j == cls_n0(p) + cls_n1(p))) {
+        if (j == 0 || (CLS && j == p.cls_n01)) {
           m_run = m_new;
         } else if (__any_sync(0xffffffffu, m_new > m_run + RESCALE_LOG2)) {
           // O_i holds P_i(0..j-1) V, all of it complete (the commit that
@@ -1314,6 +1302,7 @@ cudaError_t launch_d(const TcArgs& a, int ctas, cudaStream_t s) {
 }  // namespace
 
 int tc_block_rows() { return QT * BM; }
+int tc_key_tile() { return BN; }
 
 int device_sm_count() {
   constexpr int kMaxDevices = 128;

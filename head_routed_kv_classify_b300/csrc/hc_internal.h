@@ -255,6 +255,8 @@ struct AttnParams {
   // writes the per-token statistics.
   int32_t cls;
   int32_t seg_sink, seg_dummy;
+  int32_t cls_n0, cls_n01;          // first key tile of the middle / the Dummy segment
+  int32_t cls_v0, cls_v1, cls_v2;   // keys in the last tile of each segment
   float* park_o;              // [2][Nq][H][d]: Sink state, state before the Dummy block
   float* park_ml;             // [2][Nq][H][2]
   const float* proxy_o;       // [Nq][H][d] the proxy output (normalised)
@@ -295,6 +297,7 @@ struct TcKV {
 // otherwise CTA c runs items c, c + ctas, c + 2*ctas, ...
 cudaError_t launch_attention_tc(const AttnParams& p, const TcKV& kv, int ctas, cudaStream_t s);
 int tc_block_rows();                          // queries per tcgen05 item (256)
+int tc_key_tile();                            // keys per tcgen05 key tile (128)
 int proxy_block_rows();                       // queries per classification-proxy item
 int device_sm_count();                        // SMs of the current device (cached)
 
