@@ -89,7 +89,8 @@ struct Layout {
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   static constexpr int OFF_ITEMS = OFF_BAR + 256;   // the CTA's work items (list launches)
-  static constexpr int BYTES = OFF_ITEMS + ITEM_CACHE * (int)sizeof(WorkItem);
+  static constexpr int OFF_MASK = OFF_ITEMS + ITEM_CACHE * (int)sizeof(WorkItem);   // band window masks
+  static constexpr int BYTES = OFF_MASK + 4 * QT * 32 * kMaxBoxesPerFrame * 16;
   static constexpr int ALLOC = BYTES + 1024;        // room to align the base to 1 KB
   static constexpr uint32_t COL_O = QT * BN;        // O_i at COL_O + i * D
   static_assert(COL_O + QT * D <= TMEM_COLS, "TMEM budget");
@@ -775,6 +776,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     const uint32_t t_o = t_lane + L::COL_O + grp * D;  // O_i
     const float sl2 = g.scale_log2;
     const uint32_t q_tile = sQ + grp * L::Q_BYTES;
+    const uint32_t mask_base = s_base + L::OFF_MASK + (uint32_t)(tid * kMaxBoxesPerFrame * 16);   // PROXY
     auto wait_warp = [&](int slot, uint32_t parity) -> bool {
       const bool w = mbar_wait_bounded(bar(slot), parity, abort_flag, wait_limit);
       return __all_sync(0xffffffffu, w);
@@ -840,8 +842,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     for (int w = w_begin; ok && w < w_end; w += w_step) {
       // Only what the tile loop needs stays live across it; the item is
       // decoded again for the epilogue.
-      int n, k_len, rlo = 0, rlen = 0, tpf = 1;
-      int h_lo = 0, h_hi = -1, w_lo = 0, w_hi = -1;   // PROXY: this row's key window in a frame
+      int n, k_len, tpf = 1;
       {
         const TcItem it = tc_decode(p, w, isrc);
         n = tc_tiles(p, it, CLS);
@@ -866,21 +867,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
           continue;
         }
         if (PROXY) {
-          rlo = it.rlo;
-          rlen = it.rlen;
+          // This row's window mask for each box of a key frame (the same in
+          // every frame): bit e of word e / 32 marks key column e of the box
+          // as inside the window.  Key column e of box tt is halo row
+          // tt*bh + e / kw, halo column e % kw: one run of columns per window
+          // row.
           tpf = it.tpf;
+          int h_lo, h_hi, w_lo, w_hi;
           const int pos = tc_query_token(it, g, qrow) % g.F;
           const int hq = pos / g.Fw;
           band_window(g, p.band_win, hq, pos - hq * g.Fw, h_lo, h_hi, w_lo, w_hi);
           // As offsets into the halo (rows may start before the frame; the
           // window is clipped to the frame, so it lies inside the halo).
-          h_lo -= rlo;
-          h_hi -= rlo;
-          w_lo -= rlen;
-          w_hi -= rlen;
+          h_lo -= it.rlo;
+          h_hi -= it.rlo;
+          w_lo -= it.rlen;
+          w_hi -= it.rlen;
+          const int bh = p.pg.bh, kw = p.pg.kw;
+#pragma unroll 1
+          for (int tt = 0; tt < tpf; ++tt) {
+            uint32_t m4[BN / 32];
+#pragma unroll
+            for (int q = 0; q < BN / 32; ++q) m4[q] = 0u;
+            const int r0 = tt * bh;
+            for (int hk = max(r0, h_lo); hk <= min(r0 + bh - 1, h_hi); ++hk) {
+              const int a = (hk - r0) * kw + w_lo;
+              const int b = (hk - r0) * kw + w_hi;
+#pragma unroll
+              for (int q = 0; q < BN / 32; ++q) {
+                const int lo = max(a, 32 * q), hi = min(b, 32 * q + 31);
+                if (lo <= hi) m4[q] |= (uint32_t)(((1ull << (hi - lo + 1)) - 1ull) << (lo - 32 * q));
+              }
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(mask_base + tt * 16), "r"(m4[0]), "r"(m4[1]),
+                         "r"(m4[2]), "r"(m4[3])
+                         : "memory");
+          }
         }
       }
       float m_run = -INFINITY, l_run = 0.f;
+      int tt = 0;   // PROXY: box of the current key tile within its key frame
       for (int j = 0; j < n; ++j, ++gt) {
         // S_1(gt) is signalled by key tile gt-1's EMPTY commit (the MMA
         // prologue's for gt = 0): slot (gt+1) % 2, its (gt/2)-th completion.
@@ -907,19 +933,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
         for (int q = 0; q < BN / 32; ++q) mw[q] = 0u;
         if (PROXY) {
-          // Key column e of box tt is halo row tt*bh + e / kw, halo column
-          // e % kw: one run of columns [w_lo, w_hi] per window row.
-          const int bh = p.pg.bh, kw = p.pg.kw;
-          const int r0 = (j % tpf) * bh;
-          for (int hk = max(r0, h_lo); hk <= min(r0 + bh - 1, h_hi); ++hk) {
-            const int a = (hk - r0) * kw + w_lo;
-            const int b = (hk - r0) * kw + w_hi;
-#pragma unroll
-            for (int q = 0; q < BN / 32; ++q) {
-              const int lo = max(a, 32 * q), hi = min(b, 32 * q + 31);
-              if (lo <= hi) mw[q] |= (uint32_t)(((1ull << (hi - lo + 1)) - 1ull) << (lo - 32 * q));
-            }
-          }
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(mw[0]), "=r"(mw[1]), "=r"(mw[2]), "=r"(mw[3])
+                       : "r"(mask_base + tt * 16)
+                       : "memory");
+          if (++tt == tpf) tt = 0;
         }
         // Pass 1: row max over the tile.  Without masked keys the TMEM load
         // reduces it; otherwise 8 independent partial maxima (three-input max)

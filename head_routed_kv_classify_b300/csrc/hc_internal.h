@@ -117,12 +117,16 @@ struct PatchGeom {
   int32_t cells, cpc; // patches are the deployed cells; query chunks per patch
 };
 
+// At most this many boxes per key frame: each softmax thread keeps its
+// window mask for every box of a frame in shared memory.
+constexpr int kMaxBoxesPerFrame = 4;
+
 inline bool finish_patch_geom(PatchGeom& pg) {
   if (pg.kw > 128 || pg.kw < 1 || pg.kh < 1) return false;
   pg.bh = 128 / pg.kw;
   if (pg.bh > pg.kh) pg.bh = pg.kh;
   pg.tpf = (pg.kh + pg.bh - 1) / pg.bh;
-  return true;
+  return pg.tpf <= kMaxBoxesPerFrame;
 }
 
 // Halo of a uniform patch for a window: the (2r+1) x (2r+1) neighbourhood
