@@ -35,7 +35,7 @@ STATUS_NAMES = {0: "HC_OK", 1: "HC_ERR_INVALID_ARG", 2: "HC_ERR_SHAPE", 3: "HC_E
                 4: "HC_ERR_ALIGN", 5: "HC_ERR_STATE", 6: "HC_ERR_CUDA", 7: "HC_ERR_TIMEOUT",
                 8: "HC_ERR_UNSUPPORTED", 9: "HC_ERR_SIZE"}
 MAX_HEADS = 64
-ABI_VERSION = 4                   # HC_ABI_VERSION this binding is written against
+ABI_VERSION = 5                   # HC_ABI_VERSION this binding is written against
 STATIC_SCRATCH_BYTES = 16 << 20   # HC_STATIC_SCRATCH_BYTES
 
 # Every symbol include/headcast.h declares.
@@ -80,7 +80,9 @@ class HcCacheInfo(C.Structure):
                 ("sink_present", C.c_int32), ("n_by_archetype", C.c_int32 * 4),
                 ("rows_by_archetype", C.c_int64 * 4), ("bytes", C.c_size_t),
                 ("kv_bytes", C.c_size_t), ("split_bytes", C.c_size_t),
-                ("monolithic_bytes", C.c_size_t)]
+                ("monolithic_bytes", C.c_size_t), ("n_work_items", C.c_int32),
+                ("n_split_runs", C.c_int32), ("n_split_pieces", C.c_int32), ("pad_", C.c_int32),
+                ("planned_span", C.c_int64), ("planned_total", C.c_int64)]
 
     def as_dict(self) -> dict:
         return dict(newest_block=self.newest_block, valid_frames=self.valid_frames,
@@ -88,7 +90,9 @@ class HcCacheInfo(C.Structure):
                     n_by_archetype=list(self.n_by_archetype),
                     rows_by_archetype=list(self.rows_by_archetype), bytes=self.bytes,
                     kv_bytes=self.kv_bytes, split_bytes=self.split_bytes,
-                    monolithic_bytes=self.monolithic_bytes)
+                    monolithic_bytes=self.monolithic_bytes, n_work_items=self.n_work_items,
+                    n_split_runs=self.n_split_runs, n_split_pieces=self.n_split_pieces,
+                    planned_span=self.planned_span, planned_total=self.planned_total)
 
 
 _lib = None

@@ -36,6 +36,8 @@ struct hc_cache {
   int n_cta_main, n_cta_band;
   int n_split;           // split key runs merged after the launch
   size_t split_bytes;    // partial-output workspace of the split runs
+  int n_parts;           // pieces of the split runs
+  int64_t plan_span, plan_total;   // the schedule's busiest CTA and total, key-tile steps
   hc::PatchGeom pg;      // patches of the sliding Spatial heads (tensor-core path)
   int64_t rows;
   int64_t rows_by_arch[4];
@@ -137,6 +139,8 @@ struct Plan {
   size_t off_items = 0, off_sched = 0, off_split = 0, off_k = 0, off_v = 0, off_part_o = 0, off_part_ml = 0;
   size_t bytes = 0, split_bytes = 0;
   hc::PatchGeom pg;      // patches of the sliding Spatial heads (tensor-core path)
+  int64_t span = 0;      // planned busiest CTA (main launch + band launch), key-tile steps
+  int64_t total = 0;     // planned work over all CTAs, key-tile steps
   bool ok = true;        // false: no patch geometry fits the sliding window
 };
 
@@ -194,8 +198,9 @@ int64_t lpt_makespan(std::vector<int64_t> costs, int ctas) {
 // Longest-processing-time-first assignment of items to `ctas` CTAs: items in
 // decreasing cost, each to the CTA with the least work so far.  Returns the
 // items regrouped per CTA (each CTA's in assignment order) and the ranges.
-void lpt_schedule(const Geom& g, std::vector<WorkItem>& items, int max_ctas, std::vector<int32_t>& sched,
-                  const hc::PatchGeom* pg = nullptr) {
+// The busiest CTA's cost is returned, the sum over CTAs added to *total.
+int64_t lpt_schedule(const Geom& g, std::vector<WorkItem>& items, int max_ctas, std::vector<int32_t>& sched,
+                     int64_t* total, const hc::PatchGeom* pg = nullptr) {
   const int n = (int)items.size();
   const int ctas = std::max(1, std::min(max_ctas, n));
   std::vector<int> order(n);
@@ -210,11 +215,14 @@ void lpt_schedule(const Geom& g, std::vector<WorkItem>& items, int max_ctas, std
   std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
   for (int c = 0; c < ctas; ++c) heap.push(Load(0, c));
   std::vector<std::vector<int>> lists(ctas);
+  int64_t span = 0;
   for (int i : order) {
     Load l = heap.top();
     heap.pop();
     lists[l.second].push_back(i);
     heap.push(Load(l.first + cost[i], l.second));
+    span = std::max(span, l.first + cost[i]);
+    *total += cost[i];
   }
   std::vector<WorkItem> out;
   out.reserve(n);
@@ -225,6 +233,7 @@ void lpt_schedule(const Geom& g, std::vector<WorkItem>& items, int max_ctas, std
   }
   sched[ctas] = (int32_t)out.size();
   items.swap(out);
+  return span;
 }
 
 // Cache layout, the routed work list and its schedule.
@@ -295,14 +304,20 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
     }
   }
   if (cfg.dtype == HC_BF16 && !main.empty()) {
-    // Split-KV: the longest key runs (Sink, Dummy or Global items) are cut
-    // into pieces whose partial outputs are merged after the launch, as long
-    // as that shortens the launch's busiest CTA by more than 5 %: it
-    // removes both a single item that outlasts the rest of the launch and
-    // the quantisation of a few long items over the CTAs.
+    // Split-KV: some of the longest key runs (Sink, Dummy or Global items)
+    // are cut into pieces whose partial outputs are merged after the launch,
+    // where that shortens the launch's busiest CTA by more than 5 %.  It
+    // removes both a single item that outlasts the rest of the launch and the
+    // quantisation of a few long items over the CTAs (507 equal items on 148
+    // CTAs leave 63 CTAs with a fourth item; splitting 63 of them in halves
+    // evens that out).  Searched: the m longest runs, each in c pieces.
     const int n = (int)main.size();
-    std::vector<int> chunks(n, 1), best = chunks;
-    auto costs = [&](const std::vector<int>& ch) {
+    std::vector<int> runs;
+    for (int i = 0; i < n; ++i)
+      if (main[i].kind == hc::ITEM_RANGE) runs.push_back(i);
+    std::stable_sort(runs.begin(), runs.end(),
+                     [&](int a, int b) { return run_tiles(g, main[a]) > run_tiles(g, main[b]); });
+    auto span_of = [&](const std::vector<int>& ch) {
       std::vector<int64_t> c;
       for (int i = 0; i < n; ++i) {
         const int64_t t = main[i].kind == hc::ITEM_RANGE ? run_tiles(g, main[i]) : item_cost(g, main[i]) - kItemOverhead;
@@ -310,30 +325,27 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
         // back by the merge: one more step.
         for (int k = 0; k < ch[i]; ++k) c.push_back((t + ch[i] - 1) / ch[i] + kItemOverhead + (ch[i] > 1 ? 1 : 0));
       }
-      return c;
+      return lpt_makespan(c, hc::kPlanCtas);
     };
-    int64_t best_span = lpt_makespan(costs(chunks), hc::kPlanCtas);
-    for (int iter = 0; iter < 4 * kMaxChunks; ++iter) {
-      // One more piece for every splittable item among the longest pieces.
-      int64_t top = 0;
-      for (int i = 0; i < n; ++i)
-        if (main[i].kind == hc::ITEM_RANGE && chunks[i] < kMaxChunks)
-          top = std::max(top, (run_tiles(g, main[i]) + chunks[i] - 1) / chunks[i]);
-      if (top < 8) break;   // pieces of under 8 key tiles are not worth a merge
-      bool grew = false;
-      for (int i = 0; i < n; ++i)
-        if (main[i].kind == hc::ITEM_RANGE && chunks[i] < kMaxChunks &&
-            (run_tiles(g, main[i]) + chunks[i] - 1) / chunks[i] * 100 >= top * 97) {
-          ++chunks[i];
-          grew = true;
+    std::vector<int> best(n, 1);
+    const int64_t base_span = span_of(best);
+    int64_t best_span = base_span;
+    const int nr = (int)runs.size();
+    const int step = std::max(1, nr / 64);
+    for (int c = 2; c <= kMaxChunks && nr > 0; ++c) {
+      for (int m = std::min(step, nr);; m = std::min(m + step, nr)) {
+        if ((run_tiles(g, main[runs[m - 1]]) + c - 1) / c < 8) break;   // pieces under 8 key tiles: no
+        std::vector<int> ch(n, 1);
+        for (int k = 0; k < m; ++k) ch[runs[k]] = c;
+        const int64_t s = span_of(ch);
+        if (s < best_span) {
+          best_span = s;
+          best = ch;
         }
-      if (!grew) break;
-      const int64_t span = lpt_makespan(costs(chunks), hc::kPlanCtas);
-      if (span * 100 < best_span * 95) {
-        best_span = span;
-        best = chunks;
+        if (m == nr) break;
       }
     }
+    if (best_span * 100 >= base_span * 95) best.assign(n, 1);
     std::vector<WorkItem> split;
     for (int i = 0; i < n; ++i) {
       const WorkItem& w = main[i];
@@ -361,8 +373,8 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
     }
     main.swap(split);
   }
-  lpt_schedule(g, main, hc::kPlanCtas, P.sched_main);
-  if (!band.empty()) lpt_schedule(g, band, hc::kPlanCtas, P.sched_band, &P.pg);
+  P.span = lpt_schedule(g, main, hc::kPlanCtas, P.sched_main, &P.total);
+  if (!band.empty()) P.span += lpt_schedule(g, band, hc::kPlanCtas, P.sched_band, &P.total, &P.pg);
   P.n_band = (int)band.size();
   P.items = main;
   P.items.insert(P.items.end(), band.begin(), band.end());
@@ -712,6 +724,9 @@ hc_status hc_cache_create(const hc_config* cfg, const int8_t* labels_host, void*
   c->n_cta_band = P.sched_band.empty() ? 0 : (int)P.sched_band.size() - 1;
   c->n_split = (int)P.splits.size();
   c->split_bytes = P.split_bytes;
+  c->n_parts = P.n_parts;
+  c->plan_span = P.span;
+  c->plan_total = P.total;
   c->pg = P.pg;
   c->rows = P.rows;
   for (int a = 0; a < 4; ++a) {
@@ -745,6 +760,11 @@ hc_status hc_cache_get_info(const hc_cache* c, hc_cache_info* out) {
   out->bytes = c->used;
   out->kv_bytes = 2 * (size_t)c->rows * kv_row_bytes(c->cfg);
   out->split_bytes = c->split_bytes;
+  out->n_work_items = c->n_items;
+  out->n_split_runs = c->n_split;
+  out->n_split_pieces = c->n_parts;
+  out->planned_span = c->plan_span;
+  out->planned_total = c->plan_total;
   out->monolithic_bytes = (size_t)2 * c->g.Wf * c->g.F * c->g.H * c->g.d * esize_of(c->cfg.dtype);
   return HC_OK;
 }
@@ -769,6 +789,11 @@ hc_status hc_cache_plan_info(const hc_config* cfg, const int8_t* labels_host, hc
   out->bytes = P.bytes;
   out->kv_bytes = 2 * (size_t)P.rows * kv_row_bytes(*cfg);
   out->split_bytes = P.split_bytes;
+  out->n_work_items = (int32_t)P.items.size();
+  out->n_split_runs = (int32_t)P.splits.size();
+  out->n_split_pieces = P.n_parts;
+  out->planned_span = P.span;
+  out->planned_total = P.total;
   out->monolithic_bytes = (size_t)2 * g.Wf * g.F * g.H * g.d * esize_of(cfg->dtype);
   return HC_OK;
 }

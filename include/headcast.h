@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define HC_ABI_VERSION 4
+#define HC_ABI_VERSION 5
 #define HC_MAX_HEADS 64
 
 typedef enum { HC_SINK = 0, HC_DUMMY = 1, HC_SPATIAL = 2, HC_GLOBAL = 3 } hc_archetype;
@@ -130,6 +130,14 @@ typedef struct {
   size_t split_bytes;       /* of which the routed launch's workspace for key
                                runs split across CTAs (0 if none is split)    */
   size_t monolithic_bytes;  /* bytes a [window][H][d] K+V cache would take    */
+  int32_t n_work_items;     /* work items of the routed launch(es)            */
+  int32_t n_split_runs;     /* key runs split across CTAs and merged after    */
+  int32_t n_split_pieces;   /* pieces of those runs                           */
+  int32_t pad_;
+  int64_t planned_span;     /* the schedule's busiest CTA, in key-tile steps
+                               (an item boundary counts as 6) with the window
+                               full; the band launch's added for sliding heads */
+  int64_t planned_total;    /* the same summed over all CTAs                   */
 } hc_cache_info;
 
 /* ----------------------------------------------------------------------- */

@@ -47,7 +47,7 @@ def test_library_does_not_need_libcuda(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.hc_abi_version() == hc.ABI_VERSION == 4
+    assert lib.hc_abi_version() == hc.ABI_VERSION == 5
     assert lib.hc_status_string(0) == b"ok"
     assert lib.hc_status_string(7) == b"device-side wait expired"
 
@@ -114,6 +114,28 @@ def test_long_key_runs_are_split_only_where_they_outlast_the_launch(lib, name, s
     cfg32 = hc.config_for(shape)
     cfg32.dtype = hc.HC_FP32                                  # the fp32 path never splits
     assert hc.hc_cache_plan_info(cfg32, shape.mix)["split_bytes"] == 0
+
+
+@pytest.mark.parametrize("arch", [0, 1, 3])
+def test_equal_items_are_split_just_enough_to_even_out_the_ctas(lib, arch):
+    """A 720P layer with every head on one key run (Sink, Dummy or Global):
+    12 x 43 equal items over 148 CTAs would leave 72 CTAs with one item more
+    than the rest.  The planner cuts some of the items, not all, in pieces,
+    so that the busiest CTA is within 2 % of the mean (and more than 5 %
+    below the unsplit plan), with every piece of at least 8 key tiles."""
+    import synth
+    shape = synth.SHAPES["720p"]
+    labels = [arch] * shape.n_heads
+    info = hc.hc_cache_plan_info(hc.config_for(shape), labels)
+    items = 12 * -(-shape.n_q // 256)
+    assert 0 < info["n_split_runs"] < items
+    assert info["n_work_items"] == items - info["n_split_runs"] + info["n_split_pieces"]
+    mean = info["planned_total"] / 148
+    assert info["planned_span"] <= 1.02 * mean
+    tiles = -(-(shape.n_q if arch != 3 else shape.n_k) // 128)
+    unsplit = -(-items // 148) * (tiles + 6)
+    assert info["planned_span"] * 100 < unsplit * 95
+    assert tiles // (info["n_split_pieces"] // info["n_split_runs"]) >= 8
 
 
 def test_cache_bytes_rejects_bad_labels(lib):
