@@ -486,7 +486,7 @@ hc_status hc_config_validate(const hc_config* c) {
 // max / sum, and the per-token statistics.  fp32 layers: four output planes
 // (full, Sink, Dummy, proxy) and the per-token statistics.
 struct ClassifyLayout {
-  size_t plane, off_proxy, off_park, off_park_ml, off_tok, total;
+  size_t plane, off_proxy, off_park, off_park1, off_park_ml, off_tok, total;
 };
 
 static ClassifyLayout classify_layout(const hc_config& c) {
@@ -495,13 +495,18 @@ static ClassifyLayout classify_layout(const hc_config& c) {
   L.plane = (size_t)nq * c.n_heads * c.head_dim * sizeof(float);
   const size_t tok = 4 * (size_t)c.n_heads * nq * sizeof(float);
   if (c.dtype == HC_BF16) {
+    // bf16 planes for the proxy output and the parked Sink state; the state
+    // before the Dummy block stays fp32 (the full-context output is made
+    // from it).
+    const size_t plane16 = L.plane / 2;
     L.off_proxy = 0;
-    L.off_park = round_up(L.plane, 256);
-    L.off_park_ml = round_up(L.off_park + 2 * L.plane, 256);
+    L.off_park = round_up(plane16, 256);
+    L.off_park1 = round_up(L.off_park + plane16, 256);
+    L.off_park_ml = round_up(L.off_park1 + L.plane, 256);
     L.off_tok = round_up(L.off_park_ml + 2 * (size_t)nq * c.n_heads * 2 * sizeof(float), 256);
   } else {
     L.off_proxy = 3 * L.plane;
-    L.off_park = L.off_park_ml = 0;
+    L.off_park = L.off_park1 = L.off_park_ml = 0;
     L.off_tok = round_up(4 * L.plane, 256);
   }
   L.total = round_up(L.off_tok + tok, 256);
@@ -561,6 +566,7 @@ hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const 
     pp.item_mode = hc::ITEMS_PROXY;
     pp.o = sc + CL.off_proxy;
     pp.o_plane_stride = 0;
+    pp.out_fp32 = 0;
     pp.proxy_frames = n_key_frames;
     const bool pg_ok = g.proxy_mode == HC_PROXY_CELL ? hc::make_cell_patch_geom(g, pp.pg)
                                                       : hc::choose_patch_geom(g, hc::WIN_PROXY, n_key_frames, pp.pg);
@@ -590,9 +596,10 @@ hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const 
       pc.cls_v1 = n1 > 0 ? (pc.seg_dummy - pc.seg_sink) - (n1 - 1) * kt : 0;
       pc.cls_v2 = ((int)nk - pc.seg_dummy) - (n2 - 1) * kt;
     }
-    pc.park_o = reinterpret_cast<float*>(sc + CL.off_park);
+    pc.park_o = sc + CL.off_park;
+    pc.park_o1 = reinterpret_cast<float*>(sc + CL.off_park1);
     pc.park_ml = reinterpret_cast<float*>(sc + CL.off_park_ml);
-    pc.proxy_o = reinterpret_cast<const float*>(sc + CL.off_proxy);
+    pc.proxy_o = sc + CL.off_proxy;
     pc.tok = reinterpret_cast<float*>(sc + CL.off_tok);
     pc.o_full = o_full;
     pc.out_fp32 = 0;

@@ -316,6 +316,9 @@ __device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
       : "+f"(s0), "+f"(s1)
       : "f"(a0), "f"(a1));
 }
+// The two bf16 halves of a 32-bit word as floats (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -811,21 +814,34 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     };
     // Classification pass: park this row's running state (O as it stands in
     // TMEM, unnormalised, with the row max and sum) in slot 0 (after the
-    // Sink segment) or 1 (before the Dummy segment).
+    // Sink segment; bf16) or 1 (before the Dummy segment; fp32).
     auto park = [&](int w, int slot, float m, float l) {
       const TcItem it = tc_decode(p, w, isrc);
       const bool ok = qrow < it.nq;
-      const int64_t row = ((int64_t)slot * p.nq_total + (it.q0 + qrow)) * g.H + it.head;
+      const int64_t tr = (int64_t)(it.q0 + qrow) * g.H + it.head;   // token row of a plane
+      const int64_t row = (int64_t)slot * p.nq_total * g.H + tr;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(t_o + c * 32, o);
         if (!ok) continue;
-        float4* dst = reinterpret_cast<float4*>(p.park_o + row * D + c * 32);
+        if (slot == 0) {   // bf16: feeds only the Sink cosine
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(p.park_o) + tr * D + c * 32);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]), __uint_as_float(o[4 * e + 2]),
-                               __uint_as_float(o[4 * e + 3]));
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t* x = o + 8 * e;
+            dst[e] = make_uint4(pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.park_o1 + tr * D + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                 __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+        }
       }
       if (ok) *reinterpret_cast<float2*>(p.park_ml + row * 2) = make_float2(m, l);
     };
@@ -1077,22 +1093,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         const float inv_d = l_run > 0.f ? 1.f / l_run : 0.f;
         const float cb = fb * inv_f, cd = fd * inv_f;
         float ff = 0.f, ss = 0.f, dd = 0.f, pp = 0.f, fs = 0.f, fdm = 0.f, fq = 0.f, se = 0.f;
-        const float* pa = p.park_o + row * D;
-        const float* pb = p.park_o + row1 * D;
-        const float* pq = p.proxy_o + row * D;
+        const uint4* pa = reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.park_o) + row * D);
+        const float4* pb = reinterpret_cast<const float4*>(p.park_o1 + row * D);
+        const uint4* pq = reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.proxy_o) + row * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(t_o + c * 32, o);
           if (!mine_ok) continue;
           uint32_t packed[16];
+          uint4 a8[4], q8[4];   // this chunk's 32 values of the bf16 planes
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            a8[e] = pa[c * 4 + e];
+            q8[e] = pq[c * 4 + e];
+          }
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(pa + c * 32 + 4 * e4);
-            const float4 b4 = *reinterpret_cast<const float4*>(pb + c * 32 + 4 * e4);
-            const float4 q4 = *reinterpret_cast<const float4*>(pq + c * 32 + 4 * e4);
-            const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
-            const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+            const uint32_t aw0 = (&a8[e4 / 2].x)[2 * (e4 & 1)], aw1 = (&a8[e4 / 2].x)[2 * (e4 & 1) + 1];
+            const uint32_t qw0 = (&q8[e4 / 2].x)[2 * (e4 & 1)], qw1 = (&q8[e4 / 2].x)[2 * (e4 & 1) + 1];
+            const float av[4] = {bf16_lo(aw0), bf16_hi(aw0), bf16_lo(aw1), bf16_hi(aw1)};
+            const float4 b4 = pb[c * 8 + e4];
+            const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+            const float qv[4] = {bf16_lo(qw0), bf16_hi(qw0), bf16_lo(qw1), bf16_hi(qw1)};
             float fv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {

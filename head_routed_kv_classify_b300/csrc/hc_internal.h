@@ -261,9 +261,10 @@ struct AttnParams {
   int32_t seg_sink, seg_dummy;
   int32_t cls_n0, cls_n01;          // first key tile of the middle / the Dummy segment
   int32_t cls_v0, cls_v1, cls_v2;   // keys in the last tile of each segment
-  float* park_o;              // [2][Nq][H][d]: Sink state, state before the Dummy block
+  void* park_o;               // bf16 [Nq][H][d]: the Sink state (unnormalised)
+  float* park_o1;             // [Nq][H][d]: the state before the Dummy block (unnormalised)
   float* park_ml;             // [2][Nq][H][2]
-  const float* proxy_o;       // [Nq][H][d] the proxy output (normalised)
+  const void* proxy_o;        // bf16 [Nq][H][d] the proxy output (normalised)
   float* tok;                 // [4][H][Nq]: cos sink, cos dummy, cos proxy, squared error
   void* o_full;               // nullable: the full-context output in the input dtype
   int32_t band_win;           // WIN_PROXY / WIN_SLIDING window of band items
