@@ -100,14 +100,39 @@ __device__ float block_select(const float* x, int n, int k, uint32_t* hist, int*
       if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int cum = 0, sel = 255;
-      for (int b = 0; b < 256; ++b) {
-        if (cum + (int)hist[b] > kk) { sel = b; break; }
-        cum += hist[b];
+    if (threadIdx.x < 32) {
+      // The bin holding rank kk: lane l sums bins [8l, 8l+8), an inclusive
+      // scan over the lanes finds the first lane whose running count passes
+      // kk, and that lane walks its eight bins.
+      const int lane = threadIdx.x;
+      uint32_t own[8];
+      int sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        own[j] = hist[8 * lane + j];
+        sum += (int)own[j];
       }
-      sh[0] = sel;
-      sh[1] = kk - cum;
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, incl > kk);
+      const int first = hit ? __ffs(hit) - 1 : 31;
+      if (lane == first) {
+        int cum = incl - sum, sel = 8 * lane + 7;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (cum + (int)own[j] > kk) {
+            sel = 8 * lane + j;
+            break;
+          }
+          cum += (int)own[j];
+        }
+        sh[0] = sel;
+        sh[1] = kk - cum;
+      }
     }
     __syncthreads();
     prefix |= (uint32_t)sh[0] << shift;
@@ -116,6 +141,36 @@ __device__ float block_select(const float* x, int n, int k, uint32_t* hist, int*
     __syncthreads();
   }
   return key2f(prefix);
+}
+
+// Given v = the k-th smallest of x (0-based), the (k+1)-th: v itself when
+// more than k+1 values are <= v, else the smallest value above v.  One pass.
+__device__ float block_select_next(const float* x, int n, int k, float v, uint32_t* hist, int* sh) {
+  const uint32_t kv = f2key(v);
+  int le = 0;
+  uint32_t gt = 0xffffffffu;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint32_t u = f2key(x[i]);
+    if (u <= kv) ++le;
+    else gt = min(gt, u);
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    le += __shfl_xor_sync(0xffffffffu, le, o);
+    gt = min(gt, __shfl_xor_sync(0xffffffffu, gt, o));
+  }
+  if (threadIdx.x == 0) {
+    sh[0] = 0;
+    hist[0] = 0xffffffffu;
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&sh[0], le);
+    atomicMin(&hist[0], gt);
+  }
+  __syncthreads();
+  const float r = sh[0] > k + 1 ? v : key2f(hist[0]);
+  __syncthreads();
+  return r;
 }
 
 __device__ double block_sum(double v, double* red) {
@@ -165,8 +220,9 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const ClassifyPost 
   const double pos = 0.05 * (double)(n - 1);
   const int lo = (int)floor(pos);
   const int hi = lo + 1 < n ? lo + 1 : n - 1;
-  const double vlo = block_select(cp, n, lo, hist, sh);
-  const double vhi = block_select(cp, n, hi, hist, sh);
+  const float flo = block_select(cp, n, lo, hist, sh);
+  const double vlo = flo;
+  const double vhi = hi == lo ? vlo : (double)block_select_next(cp, n, lo, flo, hist, sh);
   if (threadIdx.x == 0) {
     const double c_s = s_cs / n, c_d = s_cd / n, c_sp = s_cp / n;
     const double p5 = vlo + (pos - lo) * (vhi - vlo);
