@@ -2,8 +2,9 @@
 cache still in warm-up (window not full yet, so Global and Spatial heads see
 fewer frames and the Sink block is also the newest), the maximum head count,
 a proxy radius of 0 (each query's own position), a cell covering one axis
-only, a single-head d = 64 layer, and key runs split across CTAs whose
-pieces are empty while the window fills."""
+only, a single-head d = 64 layer, key runs split across CTAs whose pieces
+are empty while the window fills, and a classification whose per-token
+values are all tied."""
 import numpy as np
 import pytest
 
@@ -142,4 +143,27 @@ def test_split_key_runs_with_empty_pieces_during_warm_up():
             o = gu.to_host(cache.routed_attention(gu.to_dev(q, "bf16")))
             want = ref.routed_attention(q.values, cache_ref, labels)
             gu.assert_close(o, want, "bf16", f"split runs after block {b}")
+    hc.hc_get_last_error()
+
+
+def test_classification_with_every_token_tied():
+    """Every query of a head the same vector and a proxy neighbourhood that
+    covers the whole frame: every token of a head has the same four output
+    rows, so its per-token cosines are exactly equal on the GPU (the 5th
+    percentile is taken over ties: its two ranks are one value), and the
+    proxy equals full attention, so the proxy cosine and P5 are 1 and the
+    MSE 0 in the oracle.  Labels as the oracle's (the planted Sink and Dummy
+    heads, the other two Spatial)."""
+    shape = synth.custom_shape("tied", n_heads=4, head_dim=64, frame_h=8, frame_w=8, window_frames=12,
+                               dtype="bf16", seed=36)
+    inp = synth.make_layer(shape)
+    q = synth.Tensor3(np.repeat(inp.q.values[:1], shape.n_q, axis=0), np.repeat(inp.q.raw[:1], shape.n_q, axis=0))
+    cfg = hc.config_for(shape, proxy_radius=8)
+    labels, _, stats = hc.hc_classify(cfg, gu.to_dev(q, "bf16"), gu.to_dev(inp.k, "bf16"), gu.to_dev(inp.v, "bf16"))
+    cls = ref.classify(q.values, inp.k.values, inp.v.values, ref.geometry_of(shape, proxy_radius=8))
+    st = gu.to_host(stats)
+    assert list(labels) == list(cls.labels) == [ref.SINK, ref.DUMMY, ref.SPATIAL, ref.SPATIAL], (labels, cls.labels)
+    np.testing.assert_allclose(cls.stats[:, 2:4], 1.0, atol=1e-12)       # c_spatial and P5 in the oracle
+    np.testing.assert_allclose(st[:, 2:4], cls.stats[:, 2:4], atol=1e-5)
+    np.testing.assert_allclose(st[:, 4], cls.stats[:, 4], atol=1e-6)      # MSE
     hc.hc_get_last_error()
