@@ -955,13 +955,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                        : "memory");
           if (++tt == tpf) tt = 0;
         }
-        // Pass 1: row max over the tile.  Without masked keys the TMEM load
-        // reduces it; otherwise 8 independent partial maxima (three-input max)
-        // over the masked values.
+        // Pass 1: row max over the tile, reduced by the TMEM load itself.
+        // Band tiles take it over the whole box, window or not: any value at
+        // least the window's max stabilises the softmax equally (every score of
+        // a band tile is finite -- rows outside the frame and past the box are
+        // zero keys -- and the box's max exceeds the window's by far less than
+        // the exponent range), so only the exponent pass applies the mask.  A
+        // run's partial last tile takes 8 independent partial maxima
+        // (three-input max) over its valid keys, since the rows past the run
+        // hold stale data.
         float pm[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-        if (!PROXY && full) {
+        if (full) {
 #pragma unroll
           for (int h = 0; h < BN / 64; ++h) {
             uint32_t x[64];
@@ -972,15 +978,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
           for (int h = 0; h < BN / 64; ++h) {
             uint32_t x[64];
             tmem_ld32x2(t_s + h * 64, t_s + h * 64 + 32, x);
-            if (PROXY) {
 #pragma unroll
-              for (int e = 0; e < 64; ++e)
-                if (!((mw[2 * h + e / 32] >> (e & 31)) & 1u)) x[e] = __float_as_uint(-INFINITY);
-            } else if (!full) {
-#pragma unroll
-              for (int e = 0; e < 64; ++e)
-                if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
-            }
+            for (int e = 0; e < 64; ++e)
+              if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
               pm[u] = max3f(pm[u], __uint_as_float(x[8 * u]), __uint_as_float(x[8 * u + 1]));
