@@ -246,6 +246,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
       : "r"(taddr)
       : "memory");
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : HC_R32_8(0), HC_R32_8(8)
+      : "r"(taddr)
+      : "memory");
+}
 // Two runs of 32 columns (64 registers) with one wait.
 __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr0, uint32_t taddr1, uint32_t* r) {
   asm volatile(
@@ -284,6 +292,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
       ::"r"(taddr), HC_W32_8(0), HC_W32_8(8), HC_W32_8(16), HC_W32_8(24)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), HC_W32_8(0), HC_W32_8(8)
       : "memory");
 }
 #undef HC_W32
@@ -959,36 +973,48 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         // Band tiles take it over the whole box, window or not: any value at
         // least the window's max stabilises the softmax equally (every score of
         // a band tile is finite -- rows outside the frame and past the box are
-        // zero keys -- and the box's max exceeds the window's by far less than
-        // the exponent range), so only the exponent pass applies the mask.  A
-        // run's partial last tile takes 8 independent partial maxima
-        // (three-input max) over its valid keys, since the rows past the run
-        // hold stale data.
+        // zero keys of the same head -- and the box's max exceeds the window's
+        // by far less than the exponent range), so only the exponent pass
+        // applies the mask.  A run's partial last tile takes 8 independent
+        // partial maxima (three-input max) over its valid keys: the rows past
+        // the run may hold another head's keys.
+        // Keys [64, 128) are read first and only for their max; the scores of
+        // keys [0, 64) stay in registers for pass 2 (band tiles, whose masking
+        // needs the registers, read them again), whose probabilities then
+        // overwrite only columns already read.
         float pm[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-        if (full) {
+        auto max_tree = [&](const uint32_t* x) {
 #pragma unroll
-          for (int h = 0; h < BN / 64; ++h) {
-            uint32_t x[64];
-            pm[h] = tmem_ld64_max(t_s + h * 64, x);
+          for (int u = 0; u < 8; ++u) {
+            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u]), __uint_as_float(x[8 * u + 1]));
+            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 2]), __uint_as_float(x[8 * u + 3]));
+            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 4]), __uint_as_float(x[8 * u + 5]));
+            pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 6]), __uint_as_float(x[8 * u + 7]));
           }
-        } else {
-#pragma unroll
-          for (int h = 0; h < BN / 64; ++h) {
+        };
+        uint32_t x0[64];   // scores of keys [0, 64)
+        if (full) {
+          {
             uint32_t x[64];
-            tmem_ld32x2(t_s + h * 64, t_s + h * 64 + 32, x);
+            pm[1] = tmem_ld64_max(t_s + 64, x);
+          }
+          pm[0] = tmem_ld64_max(t_s, x0);
+        } else {
+          {
+            uint32_t x[64];
+            tmem_ld32x2(t_s + 64, t_s + 96, x);
 #pragma unroll
             for (int e = 0; e < 64; ++e)
-              if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              pm[u] = max3f(pm[u], __uint_as_float(x[8 * u]), __uint_as_float(x[8 * u + 1]));
-              pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 2]), __uint_as_float(x[8 * u + 3]));
-              pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 4]), __uint_as_float(x[8 * u + 5]));
-              pm[u] = max3f(pm[u], __uint_as_float(x[8 * u + 6]), __uint_as_float(x[8 * u + 7]));
-            }
+              if (64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
+            max_tree(x);
           }
+          tmem_ld32x2(t_s, t_s + 32, x0);
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e >= valid) x0[e] = __float_as_uint(-INFINITY);
+          max_tree(x0);
         }
         pm[0] = max3f(pm[0], pm[1], pm[2]);
         pm[3] = max3f(pm[3], pm[4], pm[5]);
@@ -998,44 +1024,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
           m_run = m_new;
         } else if (__any_sync(0xffffffffu, m_new > m_run + RESCALE_LOG2)) {
           // O_i holds P_i(0..j-1) V, all of it complete (the commit that
-          // signalled S_i(j) covers it): scale this warp's rows to the new max.
+          // signalled S_i(j) covers it): scale this warp's rows to the new max,
+          // 16 columns at a time (the kept scores are live).
           // (A row still without any unmasked key keeps m = -inf and alpha 1.)
           const float alpha = m_new == -INFINITY ? 1.f : ex2(m_run - m_new);
           l_run *= alpha;
           m_run = m_new;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(t_o + c * 32, o);
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld16(t_o + c * 16, o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(t_o + c * 32, o);
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(t_o + c * 16, o);
           }
           tmem_wait_st();
         }
         // Pass 2: probabilities 2^(s*scale*log2e - m), 64 keys at a time,
-        // packed two per column into P_i.  Masked keys become -inf, whose
-        // exponent is 0.
+        // packed two per column into P_i (keys [64h, 64h+64) to columns
+        // [32h, 32h+32)).  Masked keys become -inf, whose exponent is 0.
         // A row whose keys have all been masked so far keeps m = -inf; its
         // probabilities are all 0 (exponent of -inf), not NaN.
         const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
         float ps[8];   // 4 independent pairs of partial sums
 #pragma unroll
         for (int u = 0; u < 8; ++u) ps[u] = 0.f;
-#pragma unroll
-        for (int h = 0; h < BN / 64; ++h) {
-          // Keys [64h, 64h+64) of S_i; their probabilities go to P_i columns
-          // [32h, 32h+32), which lie inside S_i columns already read.
-          uint32_t x[64];
-          tmem_ld32x2(t_s + h * 64, t_s + h * 64 + 32, x);
+        auto exponents = [&](uint32_t* x, int h) {
           if (PROXY) {
 #pragma unroll
             for (int e = 0; e < 64; ++e)
               if (!((mw[2 * h + e / 32] >> (e & 31)) & 1u)) x[e] = __float_as_uint(-INFINITY);
-          } else if (!full) {
-#pragma unroll
-            for (int e = 0; e < 64; ++e)
-              if (h * 64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
           }
           uint32_t pk[32];
 #pragma unroll
@@ -1047,6 +1065,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             pk[c] = pack_bf16(e0, e1);
           }
           tmem_st32(t_s + h * 32, pk);
+        };
+        if (PROXY) tmem_ld32x2(t_s, t_s + 32, x0);
+        exponents(x0, 0);
+        {
+          uint32_t x[64];
+          tmem_ld32x2(t_s + 64, t_s + 96, x);
+          if (!full) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (64 + e >= valid) x[e] = __float_as_uint(-INFINITY);
+          }
+          exponents(x, 1);
         }
         l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         tmem_wait_st();
