@@ -26,7 +26,9 @@
 //              each barrier poll between two MMA batches leaves the tensor
 //              pipe idle, since an MMA issue returns only once the pipe
 //              accepts it.
-//   warp 9     MMA issuer, in the order P_0 V, S_0, P_1 V, S_1 per key tile,
+//   warp 9     MMA issuer (the whole warp runs the loop with warp-uniform
+//              descriptors; one elected lane issues), in the order
+//              P_0 V, S_0, P_1 V, S_1 per key tile,
 //              so the tensor core always has the other tile's products
 //              queued while a softmax group works.  S uses Q and K from
 //              shared memory; P V reads P from TMEM and V from shared memory.
@@ -211,10 +213,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
          ((uint32_t)(M >> 4) << 24);
 }
 
+// The MMA and commit wrappers are executed by the whole issuing warp, with
+// warp-uniform operands; elect.sync picks the one lane that issues.
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      "{\n .reg .pred e, p;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
       ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -222,12 +227,14 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a, uint64_
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      "{\n .reg .pred e, p;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
       ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+               " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
                : "memory");
 }
 
@@ -682,7 +689,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     __syncwarp();
   } else if (warp == W_MMA) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t ID_S = idesc_bf16(BM, BN, false);
       constexpr uint32_t ID_PV = idesc_bf16(BM, D, true);
       // Descriptors of query tile 0 and of the first K and V stage; the
@@ -691,8 +698,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
       const uint64_t dq0 = sdesc(sQ, 16, 1024);
       const uint64_t dk0 = sdesc(sK, 16, 1024);
       const uint64_t dv0 = sdesc(sV, L::KV_REG, 1024);
+      // Every lane polls (the warp stays converged) and the warp agrees.
       auto wait1 = [&](int slot, uint32_t parity) {
-        return mbar_wait_bounded(bar(slot), parity, abort_flag, wait_limit);
+        const bool r = mbar_wait_bounded(bar(slot), parity, abort_flag, wait_limit);
+        return __all_sync(0xffffffffu, r);
       };
       // S_i = Q_i K(t)^T into S_i's TMEM columns (t: global key tile).
       auto mma_s = [&](int i, int t) {
