@@ -598,6 +598,10 @@ hc_status hc_classify(const hc_config* cfg, const void* q, const void* k, const 
     }
     pc.park_o = sc + CL.off_park;
     pc.park_o1 = reinterpret_cast<float*>(sc + CL.off_park1);
+    // The state before the Dummy block builds the full-context output: fp32
+    // when the caller wants that output, else bf16 (it then feeds only the
+    // cosines and squared errors, as the parked Sink state does).
+    pc.park1_bf16 = o_full ? 0 : 1;
     pc.park_ml = reinterpret_cast<float*>(sc + CL.off_park_ml);
     pc.proxy_o = sc + CL.off_proxy;
     pc.tok = reinterpret_cast<float*>(sc + CL.off_tok);

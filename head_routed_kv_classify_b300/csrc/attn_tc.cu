@@ -837,7 +837,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     };
     // Classification pass: park this row's running state (O as it stands in
     // TMEM, unnormalised, with the row max and sum) in slot 0 (after the
-    // Sink segment; bf16) or 1 (before the Dummy segment; fp32).
+    // Sink segment; bf16) or 1 (before the Dummy segment; fp32 when the
+    // full-context output is wanted, else bf16).
     auto park = [&](int w, int slot, float m, float l) {
       const TcItem it = tc_decode(p, w, isrc);
       const bool ok = qrow < it.nq;
@@ -848,8 +849,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         uint32_t o[32];
         tmem_ld32(t_o + c * 32, o);
         if (!ok) continue;
-        if (slot == 0) {   // bf16: feeds only the Sink cosine
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(p.park_o) + tr * D + c * 32);
+        if (slot == 0 || p.park1_bf16) {   // bf16: feeds only the cosines
+          uint4* dst = reinterpret_cast<uint4*>((slot == 0 ? static_cast<bf16*>(p.park_o)
+                                                           : reinterpret_cast<bf16*>(p.park_o1)) +
+                                                tr * D + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const uint32_t* x = o + 8 * e;
@@ -1134,6 +1137,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         float ff = 0.f, ss = 0.f, dd = 0.f, pp = 0.f, fs = 0.f, fdm = 0.f, fq = 0.f, se = 0.f;
         const uint4* pa = reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.park_o) + row * D);
         const float4* pb = reinterpret_cast<const float4*>(p.park_o1 + row * D);
+        const uint4* pb16 = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(p.park_o1) + row * D);
         const uint4* pq = reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.proxy_o) + row * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -1141,19 +1145,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
           tmem_ld32(t_o + c * 32, o);
           if (!mine_ok) continue;
           uint32_t packed[16];
-          uint4 a8[4], q8[4];   // this chunk's 32 values of the bf16 planes
+          uint4 a8[4], q8[4], b8[4];   // this chunk's 32 values of the bf16 planes
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             a8[e] = pa[c * 4 + e];
             q8[e] = pq[c * 4 + e];
+            b8[e] = p.park1_bf16 ? pb16[c * 4 + e] : make_uint4(0u, 0u, 0u, 0u);
           }
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const uint32_t aw0 = (&a8[e4 / 2].x)[2 * (e4 & 1)], aw1 = (&a8[e4 / 2].x)[2 * (e4 & 1) + 1];
             const uint32_t qw0 = (&q8[e4 / 2].x)[2 * (e4 & 1)], qw1 = (&q8[e4 / 2].x)[2 * (e4 & 1) + 1];
             const float av[4] = {bf16_lo(aw0), bf16_hi(aw0), bf16_lo(aw1), bf16_hi(aw1)};
-            const float4 b4 = pb[c * 8 + e4];
-            const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+            float bv[4];
+            if (p.park1_bf16) {
+              const uint32_t bw0 = (&b8[e4 / 2].x)[2 * (e4 & 1)], bw1 = (&b8[e4 / 2].x)[2 * (e4 & 1) + 1];
+              bv[0] = bf16_lo(bw0);
+              bv[1] = bf16_hi(bw0);
+              bv[2] = bf16_lo(bw1);
+              bv[3] = bf16_hi(bw1);
+            } else {
+              const float4 b4 = pb[c * 8 + e4];
+              bv[0] = b4.x;
+              bv[1] = b4.y;
+              bv[2] = b4.z;
+              bv[3] = b4.w;
+            }
             const float qv[4] = {bf16_lo(qw0), bf16_hi(qw0), bf16_lo(qw1), bf16_hi(qw1)};
             float fv[4];
 #pragma unroll

@@ -262,7 +262,9 @@ struct AttnParams {
   int32_t cls_n0, cls_n01;          // first key tile of the middle / the Dummy segment
   int32_t cls_v0, cls_v1, cls_v2;   // keys in the last tile of each segment
   void* park_o;               // bf16 [Nq][H][d]: the Sink state (unnormalised)
-  float* park_o1;             // [Nq][H][d]: the state before the Dummy block (unnormalised)
+  float* park_o1;             // [Nq][H][d]: the state before the Dummy block (unnormalised);
+                              // bf16 (in the same area) when park1_bf16 is set
+  int32_t park1_bf16;         // no full-context output wanted: the cosines alone read it
   float* park_ml;             // [2][Nq][H][2]
   const void* proxy_o;        // bf16 [Nq][H][d] the proxy output (normalised)
   float* tok;                 // [4][H][Nq]: cos sink, cos dummy, cos proxy, squared error
