@@ -35,7 +35,7 @@ STATUS_NAMES = {0: "HC_OK", 1: "HC_ERR_INVALID_ARG", 2: "HC_ERR_SHAPE", 3: "HC_E
                 4: "HC_ERR_ALIGN", 5: "HC_ERR_STATE", 6: "HC_ERR_CUDA", 7: "HC_ERR_TIMEOUT",
                 8: "HC_ERR_UNSUPPORTED", 9: "HC_ERR_SIZE"}
 MAX_HEADS = 64
-ABI_VERSION = 5                   # HC_ABI_VERSION this binding is written against
+ABI_VERSION = 6                   # HC_ABI_VERSION this binding is written against
 STATIC_SCRATCH_BYTES = 16 << 20   # HC_STATIC_SCRATCH_BYTES
 
 # Every symbol include/headcast.h declares.
@@ -43,7 +43,8 @@ EXPORTS = ("hc_abi_version", "hc_status_string", "hc_last_error_message", "hc_co
            "hc_config_validate", "hc_classify_scratch_bytes", "hc_classify", "hc_cache_bytes",
            "hc_cache_create", "hc_cache_destroy", "hc_cache_get_info", "hc_cache_restructure",
            "hc_cache_append", "hc_routed_attention", "hc_full_attention", "hc_get_last_error",
-           "hc_classify_static_scratch", "hc_debug_inject_stall", "hc_cache_plan_info")
+           "hc_classify_static_scratch", "hc_debug_inject_stall", "hc_cache_plan_info",
+           "hc_full_attention_ws_bytes", "hc_full_attention_ws")
 
 
 class HeadcastUnavailable(RuntimeError):
@@ -128,6 +129,8 @@ def load(path: str = LIB_PATH):
         "hc_get_last_error": (C.c_int, [vp]),
         "hc_classify_static_scratch": (C.c_int, [cfgp, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
         "hc_debug_inject_stall": (C.c_int, [i32]),
+        "hc_full_attention_ws_bytes": (C.c_int, [cfgp, i32, i32, C.POINTER(sz)]),
+        "hc_full_attention_ws": (C.c_int, [cfgp, vp, vp, vp, i32, i32, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -345,16 +348,31 @@ def hc_routed_attention(cache: Cache, q, o=None, stream=None):
     return cache.routed_attention(q, o, stream)
 
 
-def hc_full_attention(cfg, q, k, v, o=None, n_key_frames=None, stream=None):
+def hc_full_attention_ws_bytes(cfg, n_q_tokens, n_key_frames) -> int:
+    n = C.c_size_t(0)
+    _check(load().hc_full_attention_ws_bytes(C.byref(cfg), n_q_tokens, n_key_frames, C.byref(n)))
+    return n.value
+
+
+def hc_full_attention(cfg, q, k, v, o=None, n_key_frames=None, stream=None, scratch=None, balanced=True):
+    """Full attention of every head over the key window.  bf16 layers use the
+    balanced schedule (hc_full_attention_ws; `scratch` is created when
+    omitted) unless balanced=False, which calls hc_full_attention."""
     nkf = k.shape[0] // cfg.F if n_key_frames is None else n_key_frames
     H, d = cfg.n_heads, cfg.head_dim
     nq = q.shape[0]
     if o is None:
         o = _torch().empty((nq, H, d), dtype=_dtype_of(cfg), device=q.device)
-    _check(load().hc_full_attention(C.byref(cfg), _ptr(q, cfg, "q", (nq, H, d)),
-                                    _ptr(k, cfg, "k", (nkf * cfg.F, H, d)),
-                                    _ptr(v, cfg, "v", (nkf * cfg.F, H, d)), nq, nkf,
-                                    _ptr(o, cfg, "o", (nq, H, d)), _stream(stream)))
+    args = (C.byref(cfg), _ptr(q, cfg, "q", (nq, H, d)), _ptr(k, cfg, "k", (nkf * cfg.F, H, d)),
+            _ptr(v, cfg, "v", (nkf * cfg.F, H, d)), nq, nkf, _ptr(o, cfg, "o", (nq, H, d)))
+    if balanced and cfg.dtype == HC_BF16 and nq > 0:
+        nbytes = hc_full_attention_ws_bytes(cfg, nq, nkf)
+        if scratch is None:
+            scratch = _torch().empty(max(nbytes, 256), dtype=_torch().uint8, device=q.device)
+        _check(load().hc_full_attention_ws(*args, _ptr(scratch, None, "scratch"),
+                                           scratch.numel() * scratch.element_size(), _stream(stream)))
+    else:
+        _check(load().hc_full_attention(*args, _stream(stream)))
     return o
 
 

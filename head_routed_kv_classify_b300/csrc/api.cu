@@ -8,6 +8,7 @@
 #include <cstring>
 #include <functional>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <queue>
 #include <string>
@@ -236,6 +237,79 @@ int64_t lpt_schedule(const Geom& g, std::vector<WorkItem>& items, int max_ctas, 
   return span;
 }
 
+// Split-KV: some of the longest key runs (Sink, Dummy or Global items) are
+// cut into pieces whose partial outputs are merged after the launch, where
+// that shortens the launch's busiest CTA by more than 5 %.  It removes both a
+// single item that outlasts the rest of the launch and the quantisation of a
+// few long items over the CTAs (507 equal items on 148 CTAs leave 63 CTAs with
+// a fourth item; splitting 63 of them in halves evens that out).  Searched:
+// the m longest runs, each in c pieces.  Pieces replace their item in `main`;
+// `splits` gets one entry per split run, `n_parts` counts the pieces.
+void split_runs(const Geom& g, std::vector<WorkItem>& main, std::vector<SplitItem>& splits, int& n_parts) {
+  if (main.empty()) return;
+  const int n = (int)main.size();
+  std::vector<int> runs;
+  for (int i = 0; i < n; ++i)
+    if (main[i].kind == hc::ITEM_RANGE) runs.push_back(i);
+  std::stable_sort(runs.begin(), runs.end(),
+                   [&](int a, int b) { return run_tiles(g, main[a]) > run_tiles(g, main[b]); });
+  auto span_of = [&](const std::vector<int>& ch) {
+    std::vector<int64_t> c;
+    for (int i = 0; i < n; ++i) {
+      const int64_t t = main[i].kind == hc::ITEM_RANGE ? run_tiles(g, main[i]) : item_cost(g, main[i]) - kItemOverhead;
+      // A piece of a split run also writes its partial output and is read
+      // back by the merge: one more step.
+      for (int k = 0; k < ch[i]; ++k) c.push_back((t + ch[i] - 1) / ch[i] + kItemOverhead + (ch[i] > 1 ? 1 : 0));
+    }
+    return lpt_makespan(c, hc::kPlanCtas);
+  };
+  std::vector<int> best(n, 1);
+  const int64_t base_span = span_of(best);
+  int64_t best_span = base_span;
+  const int nr = (int)runs.size();
+  const int step = std::max(1, nr / 64);
+  for (int c = 2; c <= kMaxChunks && nr > 0; ++c) {
+    for (int m = std::min(step, nr);; m = std::min(m + step, nr)) {
+      if ((run_tiles(g, main[runs[m - 1]]) + c - 1) / c < 8) break;   // pieces under 8 key tiles: no
+      std::vector<int> ch(n, 1);
+      for (int k = 0; k < m; ++k) ch[runs[k]] = c;
+      const int64_t s = span_of(ch);
+      if (s < best_span) {
+        best_span = s;
+        best = ch;
+      }
+      if (m == nr) break;
+    }
+  }
+  if (best_span * 100 >= base_span * 95) best.assign(n, 1);
+  std::vector<WorkItem> split;
+  for (int i = 0; i < n; ++i) {
+    const WorkItem& w = main[i];
+    const int k = best[i];
+    if (k <= 1) {
+      split.push_back(w);
+      continue;
+    }
+    SplitItem si;
+    std::memset(&si, 0, sizeof si);
+    si.head = w.head;
+    si.q0 = w.q0;
+    si.nq = w.nq;
+    si.n_chunks = k;
+    si.part0 = n_parts;
+    splits.push_back(si);
+    for (int c = 0; c < k; ++c) {
+      WorkItem x = w;
+      x.chunk = (int16_t)c;
+      x.n_chunks = (int16_t)k;
+      x.part = n_parts + c;
+      split.push_back(x);
+    }
+    n_parts += k;
+  }
+  main.swap(split);
+}
+
 // Cache layout, the routed work list and its schedule.
 void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
   const Geom g = make_geom(cfg);
@@ -303,76 +377,7 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
         }
     }
   }
-  if (cfg.dtype == HC_BF16 && !main.empty()) {
-    // Split-KV: some of the longest key runs (Sink, Dummy or Global items)
-    // are cut into pieces whose partial outputs are merged after the launch,
-    // where that shortens the launch's busiest CTA by more than 5 %.  It
-    // removes both a single item that outlasts the rest of the launch and the
-    // quantisation of a few long items over the CTAs (507 equal items on 148
-    // CTAs leave 63 CTAs with a fourth item; splitting 63 of them in halves
-    // evens that out).  Searched: the m longest runs, each in c pieces.
-    const int n = (int)main.size();
-    std::vector<int> runs;
-    for (int i = 0; i < n; ++i)
-      if (main[i].kind == hc::ITEM_RANGE) runs.push_back(i);
-    std::stable_sort(runs.begin(), runs.end(),
-                     [&](int a, int b) { return run_tiles(g, main[a]) > run_tiles(g, main[b]); });
-    auto span_of = [&](const std::vector<int>& ch) {
-      std::vector<int64_t> c;
-      for (int i = 0; i < n; ++i) {
-        const int64_t t = main[i].kind == hc::ITEM_RANGE ? run_tiles(g, main[i]) : item_cost(g, main[i]) - kItemOverhead;
-        // A piece of a split run also writes its partial output and is read
-        // back by the merge: one more step.
-        for (int k = 0; k < ch[i]; ++k) c.push_back((t + ch[i] - 1) / ch[i] + kItemOverhead + (ch[i] > 1 ? 1 : 0));
-      }
-      return lpt_makespan(c, hc::kPlanCtas);
-    };
-    std::vector<int> best(n, 1);
-    const int64_t base_span = span_of(best);
-    int64_t best_span = base_span;
-    const int nr = (int)runs.size();
-    const int step = std::max(1, nr / 64);
-    for (int c = 2; c <= kMaxChunks && nr > 0; ++c) {
-      for (int m = std::min(step, nr);; m = std::min(m + step, nr)) {
-        if ((run_tiles(g, main[runs[m - 1]]) + c - 1) / c < 8) break;   // pieces under 8 key tiles: no
-        std::vector<int> ch(n, 1);
-        for (int k = 0; k < m; ++k) ch[runs[k]] = c;
-        const int64_t s = span_of(ch);
-        if (s < best_span) {
-          best_span = s;
-          best = ch;
-        }
-        if (m == nr) break;
-      }
-    }
-    if (best_span * 100 >= base_span * 95) best.assign(n, 1);
-    std::vector<WorkItem> split;
-    for (int i = 0; i < n; ++i) {
-      const WorkItem& w = main[i];
-      const int k = best[i];
-      if (k <= 1) {
-        split.push_back(w);
-        continue;
-      }
-      SplitItem si;
-      std::memset(&si, 0, sizeof si);
-      si.head = w.head;
-      si.q0 = w.q0;
-      si.nq = w.nq;
-      si.n_chunks = k;
-      si.part0 = P.n_parts;
-      P.splits.push_back(si);
-      for (int c = 0; c < k; ++c) {
-        WorkItem x = w;
-        x.chunk = (int16_t)c;
-        x.n_chunks = (int16_t)k;
-        x.part = P.n_parts + c;
-        split.push_back(x);
-      }
-      P.n_parts += k;
-    }
-    main.swap(split);
-  }
+  if (cfg.dtype == HC_BF16) split_runs(g, main, P.splits, P.n_parts);
   P.span = lpt_schedule(g, main, hc::kPlanCtas, P.sched_main, &P.total);
   if (!band.empty()) P.span += lpt_schedule(g, band, hc::kPlanCtas, P.sched_band, &P.total, &P.pg);
   P.n_band = (int)band.size();
@@ -388,6 +393,61 @@ void plan_cache(const hc_config& cfg, const int8_t* labels, Plan& P) {
   P.off_part_ml = round_up(P.off_part_o + (size_t)P.n_parts * hc::kPartRows * g.d * sizeof(float), 256);
   P.bytes = round_up(P.off_part_ml + (size_t)P.n_parts * hc::kPartRows * 2 * sizeof(float), 256);
   P.split_bytes = P.bytes - P.off_part_o;
+}
+
+// Full attention's balanced schedule: every head's queries in 256-query
+// items over the whole key window, dealt longest-first with long runs split
+// (the routed launch's planner), and the workspace that holds the list, the
+// schedule, the split table and the pieces' partial outputs.  Planning takes
+// milliseconds, so plans are kept per shape.
+struct FullPlan {
+  std::vector<WorkItem> items;
+  std::vector<int32_t> sched;
+  std::vector<SplitItem> splits;
+  int n_parts = 0;
+  size_t off_items = 0, off_sched = 0, off_split = 0, off_part_o = 0, off_part_ml = 0, bytes = 0;
+};
+
+std::shared_ptr<const FullPlan> full_plan(const hc_config& cfg, int32_t n_q_tokens, int32_t n_key_frames) {
+  static std::mutex mu;
+  static std::map<std::vector<int64_t>, std::shared_ptr<const FullPlan>> plans;
+  const std::vector<int64_t> key = {cfg.n_heads, cfg.head_dim, cfg.frame_h, cfg.frame_w, cfg.frames_per_block,
+                                    cfg.window_frames, n_q_tokens, n_key_frames};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = plans.find(key);
+    if (it != plans.end()) return it->second;
+  }
+  const Geom g = make_geom(cfg);
+  const int BM = hc::attention_block_rows(cfg.dtype, cfg.head_dim);
+  const int64_t nk = (int64_t)n_key_frames * g.F;
+  auto P = std::make_shared<FullPlan>();
+  for (int h = 0; h < g.H; ++h)
+    for (int q0 = 0; q0 < n_q_tokens; q0 += BM) {
+      WorkItem w;
+      std::memset(&w, 0, sizeof w);
+      w.head = h;
+      w.kind = hc::ITEM_RANGE;
+      w.q0 = q0;
+      w.nq = std::min(BM, n_q_tokens - q0);
+      w.k_row0 = 0;
+      w.k_len = (int32_t)nk;
+      w.n_chunks = 1;
+      w.part = -1;
+      P->items.push_back(w);
+    }
+  split_runs(g, P->items, P->splits, P->n_parts);
+  int64_t total = 0;
+  lpt_schedule(g, P->items, hc::kPlanCtas, P->sched, &total);
+  P->off_items = 0;
+  P->off_sched = round_up(P->items.size() * sizeof(WorkItem), 256);
+  P->off_split = round_up(P->off_sched + P->sched.size() * sizeof(int32_t), 256);
+  P->off_part_o = round_up(P->off_split + P->splits.size() * sizeof(SplitItem), 256);
+  P->off_part_ml = round_up(P->off_part_o + (size_t)P->n_parts * hc::kPartRows * g.d * sizeof(float), 256);
+  P->bytes = round_up(P->off_part_ml + (size_t)P->n_parts * hc::kPartRows * 2 * sizeof(float), 256);
+  std::lock_guard<std::mutex> lock(mu);
+  plans[key] = P;
+  return P;
 }
 
 }  // namespace
@@ -973,6 +1033,87 @@ hc_status hc_full_attention(const hc_config* cfg, const void* q, const void* k, 
             "full attention");
   } else {
     HC_CUDA(hc::launch_attention(p, cfg->dtype, grid, static_cast<cudaStream_t>(stream)), "full attention");
+  }
+  return HC_OK;
+}
+
+hc_status hc_full_attention_ws_bytes(const hc_config* cfg, int32_t n_q_tokens, int32_t n_key_frames,
+                                     size_t* bytes) {
+  hc_status s = hc_config_validate(cfg);
+  if (s != HC_OK) return s;
+  if (!bytes) return fail(HC_ERR_INVALID_ARG, "bytes is null");
+  if (n_q_tokens < 0 || n_key_frames < 1 || n_key_frames > 4096)
+    return fail(HC_ERR_SHAPE, "n_q_tokens %d / n_key_frames %d", n_q_tokens, n_key_frames);
+  *bytes = cfg->dtype == HC_BF16 && n_q_tokens > 0 ? full_plan(*cfg, n_q_tokens, n_key_frames)->bytes : 0;
+  return HC_OK;
+}
+
+hc_status hc_full_attention_ws(const hc_config* cfg, const void* q, const void* k, const void* v,
+                               int32_t n_q_tokens, int32_t n_key_frames, void* o, void* scratch,
+                               size_t scratch_bytes, void* stream) {
+  hc_status s = hc_config_validate(cfg);
+  if (s != HC_OK) return s;
+  if (cfg->dtype != HC_BF16 || n_q_tokens == 0)
+    return hc_full_attention(cfg, q, k, v, n_q_tokens, n_key_frames, o, stream);
+  if (!q || !k || !v || !o || !scratch) return fail(HC_ERR_INVALID_ARG, "null argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(scratch))
+    return fail(HC_ERR_ALIGN, "device pointers must be 16-byte aligned");
+  if (n_q_tokens < 0 || n_key_frames < 1 || n_key_frames > 4096)
+    return fail(HC_ERR_SHAPE, "n_q_tokens %d / n_key_frames %d", n_q_tokens, n_key_frames);
+  const Geom g = make_geom(*cfg);
+  const int64_t nk = (int64_t)n_key_frames * g.F;
+  if (nk >= (1ll << 31)) return fail(HC_ERR_SHAPE, "too many keys");
+  const std::shared_ptr<const FullPlan> P = full_plan(*cfg, n_q_tokens, n_key_frames);
+  if (scratch_bytes < P->bytes)
+    return fail(HC_ERR_INVALID_ARG, "scratch_bytes %zu < %zu (hc_full_attention_ws_bytes)", scratch_bytes, P->bytes);
+  int* status = nullptr;
+  if ((s = status_ptr(&status)) != HC_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(scratch);
+  // The plan into the workspace (a few tens of KB; the host copies live in
+  // the plan cache).
+  HC_CUDA(cudaMemcpyAsync(ws + P->off_items, P->items.data(), P->items.size() * sizeof(WorkItem),
+                          cudaMemcpyHostToDevice, st),
+          "full attention work list upload");
+  HC_CUDA(cudaMemcpyAsync(ws + P->off_sched, P->sched.data(), P->sched.size() * sizeof(int32_t),
+                          cudaMemcpyHostToDevice, st),
+          "full attention schedule upload");
+  if (!P->splits.empty())
+    HC_CUDA(cudaMemcpyAsync(ws + P->off_split, P->splits.data(), P->splits.size() * sizeof(SplitItem),
+                            cudaMemcpyHostToDevice, st),
+            "full attention split table upload");
+  hc::AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.k_stride = (int64_t)g.H * g.d;
+  p.k_hstride = g.d;
+  p.nq_total = n_q_tokens;
+  p.out_fp32 = 0;
+  p.item_mode = hc::ITEMS_LIST;
+  p.items = reinterpret_cast<const WorkItem*>(ws + P->off_items);
+  p.n_items = (int)P->items.size();
+  p.sched = reinterpret_cast<const int32_t*>(ws + P->off_sched);
+  p.part_o = reinterpret_cast<float*>(ws + P->off_part_o);
+  p.part_ml = reinterpret_cast<float*>(ws + P->off_part_ml);
+  p.valid_frames = n_key_frames;
+  p.g = g;
+  p.status = status;
+  const hc::TcKV kv{k, v, g.H, nk};
+  HC_CUDA(hc::launch_attention_tc(p, kv, (int)P->sched.size() - 1, st), "full attention");
+  if (!P->splits.empty()) {
+    hc::CombineParams m;
+    std::memset(&m, 0, sizeof m);
+    m.items = reinterpret_cast<const SplitItem*>(ws + P->off_split);
+    m.n_items = (int)P->splits.size();
+    m.out_fp32 = 0;
+    m.part_o = p.part_o;
+    m.part_ml = p.part_ml;
+    m.o = o;
+    m.g = g;
+    HC_CUDA(hc::launch_combine(m, st), "full attention (split-run merge)");
   }
   return HC_OK;
 }

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define HC_ABI_VERSION 5
+#define HC_ABI_VERSION 6
 #define HC_MAX_HEADS 64
 
 typedef enum { HC_SINK = 0, HC_DUMMY = 1, HC_SPATIAL = 2, HC_GLOBAL = 3 } hc_archetype;
@@ -296,6 +296,23 @@ hc_status hc_routed_attention(const hc_cache* cache, const void* q, void* o, voi
  * n_q_tokens = 0 is a no-op (the pointers may then be null). */
 hc_status hc_full_attention(const hc_config* cfg, const void* q, const void* k, const void* v,
                             int32_t n_q_tokens, int32_t n_key_frames, void* o, void* stream);
+
+/* Full attention with a caller-owned workspace, for bf16 layers: the work is
+ * planned like the routed launch -- 256-query items of every head over the
+ * whole key window, dealt longest-first to the CTAs, with as many key runs
+ * split across CTAs (and merged by a light second launch) as evens out the
+ * CTAs -- instead of a plain strided assignment.  Plans are kept per shape
+ * on the host and copied into the workspace at each call (a few tens of KB).
+ * fp32 layers run as hc_full_attention (the workspace is then unused and may
+ * be null).  Calls sharing a workspace must not overlap.  Async.
+ * scratch  device workspace of at least hc_full_attention_ws_bytes() bytes,
+ *          16-byte aligned, owned by the caller, contents undefined after the
+ *          call; HC_ERR_INVALID_ARG if smaller. */
+hc_status hc_full_attention_ws_bytes(const hc_config* cfg, int32_t n_q_tokens, int32_t n_key_frames,
+                                     size_t* bytes);
+hc_status hc_full_attention_ws(const hc_config* cfg, const void* q, const void* k, const void* v,
+                               int32_t n_q_tokens, int32_t n_key_frames, void* o, void* scratch,
+                               size_t scratch_bytes, void* stream);
 
 /* Test hook for the failure path (no counterpart in the paper).  While
  * enabled (enable != 0), every tensor-core attention launch (routed, full

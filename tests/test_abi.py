@@ -41,13 +41,20 @@ def test_library_exports_every_declared_symbol(lib):
         assert getattr(lib, name) is not None
 
 
+def test_every_export_has_declared_argument_types(lib):
+    """ctypes passes undeclared integer arguments as C int: a size_t or a
+    64-bit value would arrive truncated."""
+    for name in hc.EXPORTS:
+        assert getattr(lib, name).argtypes is not None, name
+
+
 def test_library_does_not_need_libcuda(lib):
     out = subprocess.run(["ldd", hc.LIB_PATH], capture_output=True, text=True).stdout
     assert "libcuda.so" not in out and "libcudart.so" not in out
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.hc_abi_version() == hc.ABI_VERSION == 5
+    assert lib.hc_abi_version() == hc.ABI_VERSION == 6
     assert lib.hc_status_string(0) == b"ok"
     assert lib.hc_status_string(7) == b"device-side wait expired"
 
@@ -136,6 +143,29 @@ def test_equal_items_are_split_just_enough_to_even_out_the_ctas(lib, arch):
     unsplit = -(-items // 148) * (tiles + 6)
     assert info["planned_span"] * 100 < unsplit * 95
     assert tiles // (info["n_split_pieces"] // info["n_split_runs"]) >= 8
+
+
+def test_full_attention_workspace_holds_a_balanced_plan(lib):
+    """The balanced full attention of a 720P layer (12 x 43 items of the
+    whole 75 600-key window over 148 CTAs) splits some key runs: its
+    workspace holds at least two pieces' partial outputs (256 rows x d fp32
+    plus the row max and sum each).  fp32 layers need no workspace, and the
+    sizes are checked like the call's."""
+    import synth
+    shape = synth.SHAPES["720p"]
+    cfg = hc.config_for(shape)
+    n = hc.hc_full_attention_ws_bytes(cfg, shape.n_q, shape.window_frames)
+    assert n >= 2 * 256 * (shape.head_dim + 2) * 4
+    assert n == hc.hc_full_attention_ws_bytes(cfg, shape.n_q, shape.window_frames)   # the kept plan
+    cfg32 = hc.config_for(shape)
+    cfg32.dtype = hc.HC_FP32
+    assert hc.hc_full_attention_ws_bytes(cfg32, shape.n_q, shape.window_frames) == 0
+    with pytest.raises(hc.HeadcastError) as e:
+        hc.hc_full_attention_ws_bytes(cfg, shape.n_q, 0)
+    assert e.value.name == "HC_ERR_SHAPE"
+    p = C.c_void_p(0x10000)
+    assert lib.hc_full_attention_ws(C.byref(cfg), p, p, p, shape.n_q, shape.window_frames, p, p, 256,
+                                    None) == 1   # workspace too small: rejected before any launch
 
 
 def test_cache_bytes_rejects_bad_labels(lib):
