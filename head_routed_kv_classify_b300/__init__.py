@@ -35,7 +35,7 @@ STATUS_NAMES = {0: "HC_OK", 1: "HC_ERR_INVALID_ARG", 2: "HC_ERR_SHAPE", 3: "HC_E
                 4: "HC_ERR_ALIGN", 5: "HC_ERR_STATE", 6: "HC_ERR_CUDA", 7: "HC_ERR_TIMEOUT",
                 8: "HC_ERR_UNSUPPORTED", 9: "HC_ERR_SIZE"}
 MAX_HEADS = 64
-ABI_VERSION = 6                   # HC_ABI_VERSION this binding is written against
+ABI_VERSION = 7                   # HC_ABI_VERSION this binding is written against
 STATIC_SCRATCH_BYTES = 16 << 20   # HC_STATIC_SCRATCH_BYTES
 
 # Every symbol include/headcast.h declares.
@@ -44,7 +44,7 @@ EXPORTS = ("hc_abi_version", "hc_status_string", "hc_last_error_message", "hc_co
            "hc_cache_create", "hc_cache_destroy", "hc_cache_get_info", "hc_cache_restructure",
            "hc_cache_append", "hc_routed_attention", "hc_full_attention", "hc_get_last_error",
            "hc_classify_static_scratch", "hc_debug_inject_stall", "hc_cache_plan_info",
-           "hc_full_attention_ws_bytes", "hc_full_attention_ws")
+           "hc_full_attention_ws_bytes", "hc_full_attention_ws", "hc_cache_plan_items")
 
 
 class HeadcastUnavailable(RuntimeError):
@@ -96,6 +96,13 @@ class HcCacheInfo(C.Structure):
                     planned_span=self.planned_span, planned_total=self.planned_total)
 
 
+# hc_work_item, field for field (56 bytes, 8-byte aligned).
+WORK_ITEM_DTYPE = np.dtype([("head", np.int32), ("kind", np.int32), ("q0", np.int32), ("nq", np.int32),
+                            ("k_row0", np.int64), ("k_len", np.int64), ("cell", np.int32),
+                            ("chunk", np.int32), ("n_chunks", np.int32), ("part", np.int32),
+                            ("launch", np.int32), ("cta", np.int32)], align=True)
+HC_ITEM_RANGE, HC_ITEM_CELL, HC_ITEM_BAND, HC_ITEM_PATCH = 0, 1, 3, 4
+
 _lib = None
 
 
@@ -131,6 +138,7 @@ def load(path: str = LIB_PATH):
         "hc_debug_inject_stall": (C.c_int, [i32]),
         "hc_full_attention_ws_bytes": (C.c_int, [cfgp, i32, i32, C.POINTER(sz)]),
         "hc_full_attention_ws": (C.c_int, [cfgp, vp, vp, vp, i32, i32, vp, vp, sz, vp]),
+        "hc_cache_plan_items": (C.c_int, [cfgp, vp, vp, i32, C.POINTER(i32)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -395,6 +403,18 @@ def hc_cache_plan_info(cfg, labels) -> dict:
     inf = HcCacheInfo()
     _check(load().hc_cache_plan_info(C.byref(cfg), lab.ctypes.data_as(C.c_void_p), C.byref(inf)))
     return inf.as_dict()
+
+
+def hc_cache_plan_items(cfg, labels) -> np.ndarray:
+    """The routed work list hc_cache_create would write for these labels
+    (host only), in launch order, as a structured array of WORK_ITEM_DTYPE."""
+    lab = np.ascontiguousarray(np.asarray(labels, dtype=np.int8))
+    lib, n = load(), C.c_int32(0)
+    _check(lib.hc_cache_plan_items(C.byref(cfg), lab.ctypes.data_as(C.c_void_p), None, 0, C.byref(n)))
+    out = np.zeros(n.value, WORK_ITEM_DTYPE)
+    _check(lib.hc_cache_plan_items(C.byref(cfg), lab.ctypes.data_as(C.c_void_p),
+                                   out.ctypes.data_as(C.c_void_p), n.value, C.byref(n)))
+    return out
 
 
 def memory_report(cfg, labels) -> dict:

@@ -869,6 +869,51 @@ hc_status hc_cache_plan_info(const hc_config* cfg, const int8_t* labels_host, hc
   return HC_OK;
 }
 
+hc_status hc_cache_plan_items(const hc_config* cfg, const int8_t* labels_host, hc_work_item* items_host,
+                              int32_t capacity, int32_t* n_items) {
+  hc_status s = hc_config_validate(cfg);
+  if (s != HC_OK) return s;
+  if ((s = check_labels(cfg, labels_host)) != HC_OK) return s;
+  if (!n_items) return fail(HC_ERR_INVALID_ARG, "n_items is null");
+  Plan P;
+  plan_cache(*cfg, labels_host, P);
+  if (!P.ok)
+    return fail(HC_ERR_UNSUPPORTED, "the sliding Spatial window (%dx%d) is too wide for the band kernel", cfg->cell_h,
+                cfg->cell_w);
+  static_assert(HC_ITEM_RANGE == hc::ITEM_RANGE && HC_ITEM_CELL == hc::ITEM_CELL && HC_ITEM_BAND == hc::ITEM_BAND &&
+                    HC_ITEM_PATCH == hc::ITEM_PATCH,
+                "item kinds");
+  const Geom g = make_geom(*cfg);
+  const int n = (int)P.items.size();
+  *n_items = n;
+  if (!items_host) return HC_OK;
+  if (capacity < n) return fail(HC_ERR_SIZE, "the plan has %d items, capacity %d", n, capacity);
+  const int n_main = n - P.n_band;
+  for (int launch = 0; launch < 2; ++launch) {
+    const std::vector<int32_t>& sched = launch == 0 ? P.sched_main : P.sched_band;
+    const int base = launch == 0 ? 0 : n_main;
+    for (int c = 0; c + 1 < (int)sched.size(); ++c)
+      for (int i = sched[c]; i < sched[c + 1]; ++i) {
+        const WorkItem& w = P.items[base + i];
+        hc_work_item& o = items_host[base + i];
+        std::memset(&o, 0, sizeof o);
+        o.head = w.head;
+        o.kind = w.kind;
+        o.q0 = w.q0;
+        o.nq = w.nq;
+        o.k_row0 = w.k_row0;
+        o.k_len = w.k_per_frame > 0 ? (int64_t)w.k_per_frame * g.Wf : w.k_len;
+        o.cell = w.cell;
+        o.chunk = w.chunk;
+        o.n_chunks = w.n_chunks;
+        o.part = w.part;
+        o.launch = launch;
+        o.cta = c;
+      }
+  }
+  return HC_OK;
+}
+
 static hc::ScatterParams scatter_params(const hc_cache* c, const void* k, const void* v) {
   hc::ScatterParams p;
   std::memset(&p, 0, sizeof p);

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define HC_ABI_VERSION 6
+#define HC_ABI_VERSION 7
 #define HC_MAX_HEADS 64
 
 typedef enum { HC_SINK = 0, HC_DUMMY = 1, HC_SPATIAL = 2, HC_GLOBAL = 3 } hc_archetype;
@@ -139,6 +139,46 @@ typedef struct {
                                full; the band launch's added for sliding heads */
   int64_t planned_total;    /* the same summed over all CTAs                   */
 } hc_cache_info;
+
+/* Kinds of routed work items. */
+typedef enum {
+  HC_ITEM_RANGE = 0,   /* queries q0 .. q0+nq-1 of the block (block-local
+                          tokens) against one contiguous key run: Sink,
+                          Dummy and Global heads                            */
+  HC_ITEM_CELL = 1,    /* query ordinals q0 .. q0+nq-1 of one deployed cell
+                          (its 3-frame query set in frame, row, column order)
+                          against the cell's key run: Spatial heads         */
+  HC_ITEM_BAND = 3,    /* sliding Spatial, fp32 layers: queries q0 .. q0+nq-1
+                          inside one frame, keys the band of window rows    */
+  HC_ITEM_PATCH = 4    /* sliding Spatial, bf16 layers: patch `cell` of query
+                          positions in every frame of the block (nq = 0: the
+                          patch geometry fixes its queries)                 */
+} hc_item_kind;
+
+/* One work item of a routed launch as the planner deals it (host-side view
+ * of the list hc_cache_create writes into the backing store). */
+typedef struct {
+  int32_t head;             /* head whose queries the item covers             */
+  int32_t kind;             /* hc_item_kind                                   */
+  int32_t q0, nq;           /* its queries (see hc_item_kind)                 */
+  int64_t k_row0;           /* first K (and V) row of its key run, counted in
+                               rows of the cache's per-archetype regions       */
+  int64_t k_len;            /* rows of the whole run with the window full
+                               (BAND, PATCH: the head's ring, of which the
+                               item reads its queries' windows)                */
+  int32_t cell;             /* CELL: ci * n_cells_w + cj, with
+                               n_cells_w = max(1, floor(frame_w/cell_w + 1/2))
+                               cells across a frame; PATCH: patch index        */
+  int32_t chunk, n_chunks;  /* a key run split across CTAs: this item runs key
+                               tiles [chunk*T/n_chunks, (chunk+1)*T/n_chunks)
+                               of the run's T tiles of 128 keys; n_chunks = 1:
+                               the whole run                                   */
+  int32_t part;             /* partial-output slot of a split run's piece, -1
+                               for an item that writes its output directly     */
+  int32_t launch;           /* 0: the main launch; 1: the band launch of the
+                               sliding Spatial heads                           */
+  int32_t cta;              /* the CTA of that launch the schedule gives it    */
+} hc_work_item;
 
 /* ----------------------------------------------------------------------- */
 
@@ -257,6 +297,17 @@ hc_status hc_cache_get_info(const hc_cache* cache, hc_cache_info* out);
  * steady-state memory comparison of the restructured cache with the
  * monolithic one [Pith review, Figure 9 caption / Appendix C]. */
 hc_status hc_cache_plan_info(const hc_config* cfg, const int8_t* labels_host, hc_cache_info* out);
+/* The routed work list hc_cache_create would write for these labels (HOST
+ * only, no device access), in launch order: the main launch's items CTA by
+ * CTA (each CTA's in the order it runs them), then the band launch's.  The
+ * schedule deals items longest first, each to the least loaded of 148 CTAs,
+ * after cutting the longest key runs where that shortens the busiest CTA.
+ * items_host  [capacity] hc_work_item, or null to ask only for the count.
+ * *n_items    set to the list's length in either case.
+ * HC_ERR_SIZE if items_host is given and capacity < *n_items (nothing is
+ * written to items_host then). */
+hc_status hc_cache_plan_items(const hc_config* cfg, const int8_t* labels_host, hc_work_item* items_host,
+                              int32_t capacity, int32_t* n_items);
 
 /* Fill the per-archetype regions from a monolithic window.
  * k_win, v_win  [n_blocks*3F][H][d] holding blocks first_block_id ..

@@ -54,7 +54,7 @@ def test_library_does_not_need_libcuda(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.hc_abi_version() == hc.ABI_VERSION == 6
+    assert lib.hc_abi_version() == hc.ABI_VERSION == 7
     assert lib.hc_status_string(0) == b"ok"
     assert lib.hc_status_string(7) == b"device-side wait expired"
 
